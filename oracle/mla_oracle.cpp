@@ -1,0 +1,289 @@
+// Plain fp64 CPU statement of the DeepSeek-V3.2-Exp sparse latent attention (MLA) prefill:
+// kv_norm -> wkv_b up-projection -> top-k and causal masked softmax attention.
+//
+// TEST INFRASTRUCTURE ONLY. This file is the oracle the CUDA library is checked against.
+// Only the tests, the smoke check and the benchmark's CPU-baseline leg may load it. It shares
+// no code, header, table or helper with the CUDA path, and the CUDA path never calls it.
+//
+// Sources (model atlas pages, DeepSeek-V3.2-Exp inference/model.py excerpts):
+//   * "Key-value RMSNorm" page, RMSNorm class (model.py 281-293): x.float(), mean of squares
+//     over the feature axis, x * rsqrt(var + eps), times the learned weight, eps default 1e-6.
+//   * "Key-value down-projection" page, MLA __init__ (model.py 523-539): kv_norm =
+//     RMSNorm(kv_lora_rank = 512) with the default eps; wkv_b = ColumnParallelLinear(512,
+//     n_heads * (qk_nope_head_dim + v_head_dim)); softmax_scale = qk_head_dim ** -0.5, times
+//     mscale^2 with mscale = 0.1 * args.mscale * ln(rope_factor) + 1 when max_seq_len >
+//     original_seq_len. Linear weights are held [out, in] (same page, "Parameters").
+//   * "Keys" page, MLA prefill (model.py 574-589) and ModelArgs (model.py 56-86): wkv_b output
+//     viewed [B, T, H, 256] and split [128 | 128] into k_nope and v; k = cat(k_nope, k_pe
+//     expanded over heads); scores = einsum(q, k) * softmax_scale; index mask = -inf
+//     everywhere, scattered to 0 at the top-k indices, plus the causal mask; softmax over keys;
+//     x = einsum(scores, v). max_seq_len 16384, original_seq_len 4096, rope_factor 40, mscale 1.
+//   * "Scale scores" page: S' = S * m^2 / sqrt(192), m = 1 + 0.1 ln 40, m^2 ~ 1.874.
+//
+// Readings where the pages leave a step open (each also listed in the design notes):
+//   * eps = 1e-6 (V3.2 builds RMSNorm(512) without eps; the 1e-20 printed on the V4.1 page
+//     belongs to another model).
+//   * The FP8 round trip of the latent shown in the KV-cache excerpt is not part of this path.
+//   * Causal mask: key j is allowed for query t iff j <= t (prefill from position 0).
+//   * The scatter makes the selection a set: duplicate indices count once, order is irrelevant;
+//     indices outside [0, t] are masked.
+//   * A row whose set is empty returns out = 0 and lse = -inf (the pages' softmax would be NaN).
+//   * lse = natural log of sum_j exp(s_j) over the selected keys, with s already scaled.
+//   * No intermediate rounding: every input is converted exactly to double and all arithmetic
+//     is fp64. Sums run in ascending index order.
+//
+// Build: g++ -O3 -std=c++17 -shared -fPIC -pthread mla_oracle.cpp -o libmla_oracle.so
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <thread>
+#include <vector>
+
+namespace {
+
+constexpr int kLatent = 512;   // kv_lora_rank
+constexpr int kNope = 128;     // qk_nope_head_dim
+constexpr int kRope = 64;      // qk_rope_head_dim
+constexpr int kQK = 192;       // qk_head_dim = nope + rope
+constexpr int kV = 128;        // v_head_dim
+constexpr int kKV = kNope + kV; // wkv_b output features per head
+constexpr double kRmsEps = 1e-6;
+
+// bf16 bit pattern -> double, exactly (bf16 is the upper half of an IEEE binary32).
+double bf16_bits_to_double(uint16_t bits) {
+  uint32_t u = static_cast<uint32_t>(bits) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return static_cast<double>(f);
+}
+
+// MLA __init__: qk_head_dim ** -0.5, corrected by mscale^2 for the extended context.
+double softmax_scale() {
+  const int max_seq_len = 4096 * 4;      // ModelArgs.max_seq_len
+  const int original_seq_len = 4096;     // ModelArgs.original_seq_len
+  const double rope_factor = 40.0;       // ModelArgs.rope_factor
+  const double mscale_arg = 1.0;         // ModelArgs.mscale
+  double s = std::pow(static_cast<double>(kQK), -0.5);
+  if (max_seq_len > original_seq_len) {
+    double mscale = 0.1 * mscale_arg * std::log(rope_factor) + 1.0;
+    s = s * mscale * mscale;
+  }
+  return s;
+}
+
+// RMSNorm.forward on one 512-wide row: var = mean(x^2); x * rsqrt(var + eps); weight * x.
+void kv_norm_row(const uint16_t* x_bits, const float* gamma, double* y) {
+  double x[kLatent];
+  double sum_sq = 0.0;
+  for (int c = 0; c < kLatent; ++c) {
+    x[c] = bf16_bits_to_double(x_bits[c]);
+    sum_sq += x[c] * x[c];
+  }
+  const double var = sum_sq / kLatent;
+  const double r = 1.0 / std::sqrt(var + kRmsEps);
+  for (int c = 0; c < kLatent; ++c) y[c] = static_cast<double>(gamma[c]) * (x[c] * r);
+}
+
+// Canonical selection of query t: the set {j in topk row : 0 <= j <= t}, ascending.
+// scatter_(-1, topk, 0) writes 0 once per distinct index; the causal mask removes j > t.
+void canon_row(const int32_t* idx, int K, int t, std::vector<int32_t>& sel) {
+  sel.clear();
+  for (int i = 0; i < K; ++i) {
+    const int32_t j = idx[i];
+    if (j >= 0 && j <= t) sel.push_back(j);
+  }
+  std::sort(sel.begin(), sel.end());
+  sel.erase(std::unique(sel.begin(), sel.end()), sel.end());
+}
+
+// Head h of wkv_b, transposed to [512][256] doubles: wt[c*256 + f] = W[h*256 + f][c].
+// W is [H*256, 512] ([out, in]); rows h*256 + [0,128) give k_nope, h*256 + [128,256) give v
+// (view(B, T, H, 256) then split([128, 128])).
+void head_weight_t(const uint16_t* W, int h, std::vector<double>& wt) {
+  wt.assign(static_cast<size_t>(kLatent) * kKV, 0.0);
+  for (int f = 0; f < kKV; ++f) {
+    const uint16_t* row = W + (static_cast<size_t>(h) * kKV + f) * kLatent;
+    for (int c = 0; c < kLatent; ++c) wt[static_cast<size_t>(c) * kKV + f] = bf16_bits_to_double(row[c]);
+  }
+}
+
+// One position of one head: kv[f] = sum_c W[h*256+f][c] * y[c], c ascending.
+void up_proj_row(const double* y, const double* wt, double* kv) {
+  for (int f = 0; f < kKV; ++f) kv[f] = 0.0;
+  for (int c = 0; c < kLatent; ++c) {
+    const double yc = y[c];
+    const double* w = wt + static_cast<size_t>(c) * kKV;
+    for (int f = 0; f < kKV; ++f) kv[f] += w[f] * yc;
+  }
+}
+
+template <class F>
+void parallel_for(int64_t n, int threads, F&& fn) {
+  if (threads <= 0) threads = static_cast<int>(std::thread::hardware_concurrency());
+  if (threads <= 0) threads = 1;
+  if (threads > n) threads = static_cast<int>(std::max<int64_t>(n, 1));
+  std::atomic<int64_t> next{0};
+  auto worker = [&]() {
+    for (;;) {
+      const int64_t i = next.fetch_add(1);
+      if (i >= n) break;
+      fn(i);
+    }
+  };
+  if (threads == 1) { worker(); return; }
+  std::vector<std::thread> pool;
+  for (int k = 0; k < threads; ++k) pool.emplace_back(worker);
+  for (auto& th : pool) th.join();
+}
+
+}  // namespace
+
+extern "C" {
+
+// softmax_scale of MLA __init__ (about 0.13523378).
+double oracle_softmax_scale(void) { return softmax_scale(); }
+
+// kv_norm over N rows of 512: x bf16 bits [N, 512], gamma fp32 [512] -> y fp64 [N, 512].
+void oracle_kv_norm(const uint16_t* x, const float* gamma, int64_t N, double* y) {
+  for (int64_t r = 0; r < N; ++r) kv_norm_row(x + r * kLatent, gamma, y + r * kLatent);
+}
+
+// wkv_b up-projection of N normalized rows for all H heads:
+// y fp64 [N, 512], W bf16 bits [H*256, 512] -> k_nope fp64 [N, H, 128], v fp64 [N, H, 128].
+void oracle_up_proj(const double* y, const uint16_t* W, int H, int64_t N, double* k_nope, double* v) {
+  std::vector<double> wt;
+  double kv[kKV];
+  for (int h = 0; h < H; ++h) {
+    head_weight_t(W, h, wt);
+    for (int64_t r = 0; r < N; ++r) {
+      up_proj_row(y + r * kLatent, wt.data(), kv);
+      for (int d = 0; d < kNope; ++d) k_nope[(r * H + h) * kNope + d] = kv[d];
+      for (int d = 0; d < kV; ++d) v[(r * H + h) * kV + d] = kv[kNope + d];
+    }
+  }
+}
+
+// Canonical selection of one row; writes the ascending set to sel (capacity >= K), returns n.
+int oracle_canon_row(const int32_t* idx, int K, int t, int32_t* sel) {
+  std::vector<int32_t> s;
+  canon_row(idx, K, t, s);
+  std::copy(s.begin(), s.end(), sel);
+  return static_cast<int>(s.size());
+}
+
+// The prefill path on selected query rows and heads.
+//   q      bf16 bits [B, T, H, 192] (dims 0..127 pair with k_nope, 128..191 with k_pe)
+//   c_kv   bf16 bits [B, T, 512]    (latent before kv_norm)
+//   k_pe   bf16 bits [B, T, 64]     (rotary key shared by all heads)
+//   gamma  fp32 [512]               (kv_norm weight)
+//   W      bf16 bits [H*256, 512]   (wkv_b weight, [out, in])
+//   topk   int32 [B, T, K]
+//   rows   flat row ids b*T + t, n_rows of them; NULL means all B*T rows in order
+//   heads  [h_begin, h_end)
+//   out    fp64 [n_rows, h_end - h_begin, 128];  lse fp64 [n_rows, h_end - h_begin];
+//   n_keys int32 [n_rows] (may be NULL)
+// Returns 0, or -1 on a bad argument.
+int oracle_prefill(int B, int T, int H, int K, const uint16_t* q, const uint16_t* c_kv,
+                   const uint16_t* k_pe, const float* gamma, const uint16_t* W,
+                   const int32_t* topk, int64_t n_rows, const int64_t* rows, int h_begin,
+                   int h_end, double* out, double* lse, int32_t* n_keys, int threads) {
+  if (B < 1 || T < 1 || H < 1 || K < 1 || h_begin < 0 || h_end > H || h_begin >= h_end) return -1;
+  const int64_t BT = static_cast<int64_t>(B) * T;
+  std::vector<int64_t> row_ids;
+  if (rows == nullptr) {
+    row_ids.resize(BT);
+    for (int64_t r = 0; r < BT; ++r) row_ids[r] = r;
+  } else {
+    row_ids.assign(rows, rows + n_rows);
+    for (int64_t r : row_ids)
+      if (r < 0 || r >= BT) return -1;
+  }
+  const int64_t NR = static_cast<int64_t>(row_ids.size());
+  const int HS = h_end - h_begin;
+  const double scale = softmax_scale();
+
+  // 1. Canonical selections of the requested rows.
+  std::vector<std::vector<int32_t>> sel(NR);
+  parallel_for(NR, threads, [&](int64_t i) {
+    const int64_t r = row_ids[i];
+    const int t = static_cast<int>(r % T);
+    canon_row(topk + r * K, K, t, sel[i]);
+  });
+  if (n_keys)
+    for (int64_t i = 0; i < NR; ++i) n_keys[i] = static_cast<int32_t>(sel[i].size());
+
+  // 2. kv_norm of every position any requested row can reach (j <= max t of its batch).
+  std::vector<int> tmax(B, -1);
+  for (int64_t r : row_ids) tmax[r / T] = std::max(tmax[r / T], static_cast<int>(r % T));
+  std::vector<double> y(static_cast<size_t>(BT) * kLatent, 0.0);
+  parallel_for(BT, threads, [&](int64_t r) {
+    if (static_cast<int>(r % T) <= tmax[r / T])
+      kv_norm_row(c_kv + r * kLatent, gamma, y.data() + r * kLatent);
+  });
+
+  // 3. Per (batch, head): up-project the reachable positions, then attend each requested row.
+  std::vector<std::vector<int64_t>> rows_of_batch(B);
+  for (int64_t i = 0; i < NR; ++i) rows_of_batch[row_ids[i] / T].push_back(i);
+  const int64_t units = static_cast<int64_t>(B) * HS;
+  parallel_for(units, threads, [&](int64_t u) {
+    const int b = static_cast<int>(u / HS);
+    const int h = h_begin + static_cast<int>(u % HS);
+    if (rows_of_batch[b].empty()) return;
+    std::vector<double> wt;
+    head_weight_t(W, h, wt);
+    const int npos = tmax[b] + 1;
+    std::vector<double> kv(static_cast<size_t>(npos) * kKV);  // [j][k_nope 128 | v 128]
+    for (int j = 0; j < npos; ++j)
+      up_proj_row(y.data() + (static_cast<int64_t>(b) * T + j) * kLatent, wt.data(),
+                  kv.data() + static_cast<size_t>(j) * kKV);
+    std::vector<double> s;
+    for (int64_t i : rows_of_batch[b]) {
+      const int64_t r = row_ids[i];
+      double* o = out + (i * HS + (h - h_begin)) * kV;
+      double* l = lse + i * HS + (h - h_begin);
+      const std::vector<int32_t>& S = sel[i];
+      if (S.empty()) {
+        for (int d = 0; d < kV; ++d) o[d] = 0.0;
+        *l = -std::numeric_limits<double>::infinity();
+        continue;
+      }
+      // q row of this head, and k = cat(k_nope, k_pe) for every selected key.
+      double qh[kQK];
+      const uint16_t* qrow = q + (r * H + h) * kQK;
+      for (int d = 0; d < kQK; ++d) qh[d] = bf16_bits_to_double(qrow[d]);
+      s.resize(S.size());
+      for (size_t a = 0; a < S.size(); ++a) {
+        const int j = S[a];
+        const double* kn = kv.data() + static_cast<size_t>(j) * kKV;
+        const uint16_t* kp = k_pe + (static_cast<int64_t>(b) * T + j) * kRope;
+        double dot = 0.0;
+        for (int d = 0; d < kNope; ++d) dot += qh[d] * kn[d];
+        for (int d = 0; d < kRope; ++d) dot += qh[kNope + d] * bf16_bits_to_double(kp[d]);
+        s[a] = dot * scale;
+      }
+      // softmax over the selected keys, then the value mix.
+      double M = s[0];
+      for (double x : s) M = std::max(M, x);
+      double Z = 0.0;
+      for (double& x : s) {
+        x = std::exp(x - M);
+        Z += x;
+      }
+      for (int d = 0; d < kV; ++d) o[d] = 0.0;
+      for (size_t a = 0; a < S.size(); ++a) {
+        const double* vj = kv.data() + static_cast<size_t>(S[a]) * kKV + kNope;
+        const double p = s[a];
+        for (int d = 0; d < kV; ++d) o[d] += p * vj[d];
+      }
+      for (int d = 0; d < kV; ++d) o[d] /= Z;
+      *l = M + std::log(Z);
+    }
+  });
+  return 0;
+}
+
+}  // extern "C"
