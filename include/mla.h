@@ -1,0 +1,141 @@
+/*
+ * libmla: DeepSeek-V3.2-Exp sparse latent attention (MLA) prefill on one B300 (sm_103a).
+ *
+ * The path, as the model atlas pages define it (DeepSeek-V3.2-Exp inference/model.py excerpts):
+ *   1. kv_norm: RMSNorm(512) of the key-value latent c_kv, fp32 mean of squares, eps 1e-6,
+ *      learned gain ("Key-value RMSNorm" page, RMSNorm class, model.py 281-293; MLA __init__,
+ *      model.py 523-539, on the "Key-value down-projection" page).
+ *   2. wkv_b: ColumnParallelLinear(512, H * (128 + 128)), weight [out, in]; output viewed
+ *      [B, T, H, 256] and split into k_nope (first 128) and v (last 128) ("Keys" and "Split value
+ *      heads" pages, MHA prefill, model.py 574-589).
+ *   3. k = cat(k_nope, k_pe expanded over heads) (192 features per head); scores = q . k scaled
+ *      by softmax_scale = 192^-0.5 * m^2, m = 1 + 0.1 ln 40 ("Scale scores" page; MLA __init__).
+ *   4. index mask: -inf except at the indexer's top-k positions, plus the causal mask; softmax
+ *      over keys; x = scores . v (MHA prefill, model.py 574-589).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous row-major, 16-byte
+ *     aligned. bf16 tensors are passed as mla_bf16 (the raw 16-bit pattern).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default stream). No call
+ *     synchronizes the device unless its comment says so.
+ *   - Argument and shape errors are returned synchronously and nothing is enqueued.
+ *   - Errors found on the device (a barrier wait that ran out, an index outside [0, T) when
+ *     MLA_FLAG_VALIDATE_INDICES is set) are OR-ed into a per-device status word that
+ *     mla_get_status() reads after the caller synchronizes.
+ *   - Index convention: key j is used by query t iff j occurs in topk_idx[b, t, :] and 0 <= j <= t.
+ *     Duplicates count once; order does not matter; j < 0 or j > t (including j >= T) is ignored.
+ *   - A query whose selected set is empty gets out = 0 and lse = -inf.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+typedef uint16_t mla_bf16; /* bfloat16 bit pattern */
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1, /* null pointer, misalignment, non-positive or overflowing size */
+  MLA_ERR_UNSUPPORTED = 2, /* shape outside what the kernels support (see mla_dims) */
+  MLA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+  MLA_ERR_INDEX = 4,       /* device: an index outside [0, T) under MLA_FLAG_VALIDATE_INDICES */
+  MLA_ERR_TIMEOUT = 5,     /* device: a barrier wait ran past its limit; the kernel unwound */
+  MLA_ERR_WORKSPACE = 6    /* workspace pointer misaligned or smaller than required */
+} mla_status;
+
+/* Problem sizes. The feature widths are fixed by the model: latent 512, 128 non-rotary + 64
+ * rotary query/key features, 128 value features. Supported: B >= 1, 1 <= T <= 65536,
+ * 1 <= H <= 128, K >= 1, and B*T*H*K below 2^40. */
+typedef struct {
+  int32_t B; /* batch */
+  int32_t T; /* positions (queries = keys, prefill from position 0) */
+  int32_t H; /* heads */
+  int32_t K; /* top-k width of topk_idx */
+} mla_dims;
+
+#define MLA_FLAG_VALIDATE_INDICES 1u /* report indices outside [0, T) as MLA_ERR_INDEX */
+
+/* Bytes of device workspace mla_sparse_prefill needs for `d` (0 if `d` is invalid): the
+ * up-projected keys/values kv [B, H, T, 256] fp16, the key residuals klo [B, H, T, 128] (1 byte
+ * each) and the canonical selection bitsets [B, T, ceil(T/128)*4] uint32, each 1024-byte aligned
+ * (see mla_kvnorm_wkvb and mla_canon_select for their contents). */
+MLA_API size_t mla_sparse_prefill_workspace_size(mla_dims d);
+
+/* The whole prefill path: kv_norm -> wkv_b -> sparse causal attention.
+ *   q         [B, T, H, 192] bf16: features 0..127 pair with k_nope, 128..191 (rotary, already
+ *             applied) with k_pe. Features 0..127 are used in fp16 (exact for magnitudes in
+ *             [2^-14, 65504]; smaller ones lose low bits, larger ones overflow).
+ *   c_kv      [B, T, 512] bf16: the key-value latent before kv_norm.
+ *   k_pe      [B, T, 64] bf16: the rotary key (already rotated), shared by all heads.
+ *   gamma     [512] fp32: kv_norm weight.
+ *   wkv_b     [H*256, 512] bf16, [out, in]: rows h*256 + [0,128) give k_nope of head h,
+ *             h*256 + [128,256) its v.
+ *   topk_idx  [B, T, K] int32.
+ *   out       [B, T, H, 128] bf16 (written): softmax(scale * q.k masked) . v, rounded to nearest.
+ *   lse       [B, T, H] fp32 (written): natural log of sum_j exp(scale * q.k_j) over selected j.
+ *   workspace device memory of at least mla_sparse_prefill_workspace_size(d) bytes, 1024-byte
+ *             aligned, or NULL: the call then takes it with cudaMallocAsync on `stream` and
+ *             returns it with cudaFreeAsync on the same stream.
+ * Returns MLA_OK once the work is enqueued. */
+MLA_API mla_status mla_sparse_prefill(const mla_bf16* q, const mla_bf16* c_kv, const mla_bf16* k_pe, const float* gamma,
+                              const mla_bf16* wkv_b, const int32_t* topk_idx, mla_bf16* out, float* lse,
+                              mla_dims d, void* workspace, size_t workspace_bytes, void* stream);
+
+/* As mla_sparse_prefill, plus:
+ *   n_keys  [B, T] int32 (written unless NULL): size of each query's selected key set.
+ *   flags   MLA_FLAG_VALIDATE_INDICES or 0. */
+MLA_API mla_status mla_sparse_prefill_ex(const mla_bf16* q, const mla_bf16* c_kv, const mla_bf16* k_pe, const float* gamma,
+                                 const mla_bf16* wkv_b, const int32_t* topk_idx, mla_bf16* out, float* lse,
+                                 mla_dims d, void* workspace, size_t workspace_bytes, void* stream,
+                                 int32_t* n_keys, unsigned flags);
+
+/* Stage 1 alone (the index mask of the MHA prefill excerpt, without materialising it):
+ * canonical selection bitsets. Bit (j % 32) of word sel_bits[(b*T + t)*W + j/32], W =
+ * ceil(T/128)*4, is set iff key j is selected for query t (0 <= j <= t). Words of row t at or
+ * beyond (t/128 + 1)*4 are not written. n_keys [B, T] int32 may be NULL. */
+MLA_API mla_status mla_canon_select(const int32_t* topk_idx, mla_dims d, uint32_t* sel_bits, int32_t* n_keys,
+                            unsigned flags, void* stream);
+
+/* Stages 2-3 alone: kv_norm fused into the wkv_b GEMM. For head h at position t, with k_nope and v
+ * the up-projected features (fp32 accumulation of bf16 products):
+ *   kv  [B, H, T, 256] fp16 (IEEE binary16 bit patterns): kv[.., 0:128] = k_hi = fp16(k_nope),
+ *       kv[.., 128:256] = fp16(v);
+ *   klo [B, H, T, 128] fp8 e4m3 bytes: (k_nope - k_hi) * 2^11, the part of k_nope fp16 drops.
+ * k_hi + klo * 2^-11 carries k_nope to about 2^-14 relative. |k_nope|, |v| must stay below 448. */
+MLA_API mla_status mla_kvnorm_wkvb(const mla_bf16* c_kv, const float* gamma, const mla_bf16* wkv_b, mla_dims d,
+                           uint16_t* kv, uint8_t* klo, void* stream);
+
+/* Stage 4 alone: sparse causal attention from the outputs of the two stages above. */
+MLA_API mla_status mla_sparse_attention(const mla_bf16* q, const mla_bf16* k_pe, const uint16_t* kv,
+                                const uint8_t* klo, const uint32_t* sel_bits, mla_bf16* out, float* lse,
+                                mla_dims d, void* stream);
+
+/* Device status word of the current device: MLA_OK, or the lowest error code recorded since
+ * the last mla_clear_status(). Synchronizes the current device first. */
+MLA_API mla_status mla_get_status(void);
+
+/* Reset the current device's status word to MLA_OK (synchronous). */
+MLA_API mla_status mla_clear_status(void);
+
+/* The softmax scale the kernels use: 192^-0.5 * (1 + 0.1 ln 40)^2. Host-only. */
+MLA_API double mla_softmax_scale(void);
+
+/* A static, human-readable name for a status code. Host-only. */
+MLA_API const char* mla_status_string(mla_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

@@ -29,7 +29,7 @@ LATENT, NOPE, ROPE, QK, V = 512, 128, 64, 192, 128
 def build(force: bool = False) -> str:
     """Compile mla_oracle.cpp into libmla_oracle.so next to it (g++, -O3, pthreads)."""
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
-        cmd = ["g++", "-O3", "-march=x86-64-v3", "-std=c++17", "-shared", "-fPIC", "-pthread",
+        cmd = ["g++", "-O3", "-march=x86-64-v3", "-ffp-contract=off", "-std=c++17", "-shared", "-fPIC", "-pthread",
                _SRC, "-o", _LIB_PATH + ".tmp"]
         subprocess.run(cmd, check=True)
         os.replace(_LIB_PATH + ".tmp", _LIB_PATH)
@@ -46,6 +46,10 @@ def _load():
         lib.oracle_softmax_scale.argtypes = []
         lib.oracle_kv_norm.restype = None
         lib.oracle_kv_norm.argtypes = [P, P, ctypes.c_int64, P]
+        lib.oracle_kv_norm_precast.restype = None
+        lib.oracle_kv_norm_precast.argtypes = [P, P, ctypes.c_int64, P]
+        lib.oracle_round_to_bf16.restype = None
+        lib.oracle_round_to_bf16.argtypes = [P, ctypes.c_int64, P]
         lib.oracle_up_proj.restype = None
         lib.oracle_up_proj.argtypes = [P, P, ctypes.c_int, ctypes.c_int64, P, P]
         lib.oracle_canon_row.restype = ctypes.c_int
@@ -76,16 +80,28 @@ def softmax_scale() -> float:
     return _load().oracle_softmax_scale()
 
 
-def kv_norm(x, gamma) -> np.ndarray:
-    """RMSNorm(512) with eps 1e-6 on bf16 rows ``x`` [..., 512] and fp32 ``gamma`` [512] -> fp64."""
+def kv_norm(x, gamma, precast: bool = False) -> np.ndarray:
+    """RMSNorm(512), eps 1e-6, on bf16 rows ``x`` [..., 512] with fp32 ``gamma`` [512].
+
+    Returns the bf16 output values as fp64 (the excerpt's final ``.to(dtype)``), or with
+    ``precast=True`` the fp32 values before that cast (the excerpt computes the norm in fp32)."""
     xb = _bits(x)
     shape = xb.shape
     assert shape[-1] == LATENT
     g = np.ascontiguousarray(np.asarray(gamma, dtype=np.float32))
     n = int(np.prod(shape[:-1]))
     y = np.empty((n, LATENT), dtype=np.float64)
-    _load().oracle_kv_norm(_ptr(xb), _ptr(g), n, _ptr(y))
+    fn = _load().oracle_kv_norm_precast if precast else _load().oracle_kv_norm
+    fn(_ptr(xb), _ptr(g), n, _ptr(y))
     return y.reshape(shape)
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """The oracle's round-to-nearest-even bf16 rounding, elementwise (fp64 in, fp64 out)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(x)
+    _load().oracle_round_to_bf16(_ptr(x), x.size, _ptr(y))
+    return y
 
 
 def up_proj(y: np.ndarray, W) -> tuple[np.ndarray, np.ndarray]:

@@ -29,10 +29,14 @@
 //     indices outside [0, t] are masked.
 //   * A row whose set is empty returns out = 0 and lse = -inf (the pages' softmax would be NaN).
 //   * lse = natural log of sum_j exp(s_j) over the selected keys, with s already scaled.
-//   * No intermediate rounding: every input is converted exactly to double and all arithmetic
-//     is fp64. Sums run in ascending index order.
+//   * Precision: fp64 everywhere except where the pages fix it. The RMSNorm excerpt does: it
+//     computes in fp32 (x.float()) and returns (weight * x).to(dtype), i.e. rounds the kv_norm
+//     output to bf16, the latent's dtype. The oracle does that step in fp32 in a fixed order
+//     (ascending features; IEEE sqrt and division) and rounds to bf16 (nearest, ties to even).
+//     Nothing after it is rounded: the pages do not show the Linear forward, so wkv_b's output
+//     precision is open and the oracle keeps it exact. Sums run in ascending index order.
 //
-// Build: g++ -O3 -std=c++17 -shared -fPIC -pthread mla_oracle.cpp -o libmla_oracle.so
+// Build: g++ -O3 -ffp-contract=off -std=c++17 -shared -fPIC -pthread mla_oracle.cpp -o libmla_oracle.so
 
 #include <algorithm>
 #include <atomic>
@@ -75,17 +79,41 @@ double softmax_scale() {
   return s;
 }
 
-// RMSNorm.forward on one 512-wide row: var = mean(x^2); x * rsqrt(var + eps); weight * x.
-void kv_norm_row(const uint16_t* x_bits, const float* gamma, double* y) {
-  double x[kLatent];
-  double sum_sq = 0.0;
+// Round a double to the nearest bfloat16 value (ties to even), returned as a double.
+// bfloat16 keeps 8 significant bits and float's exponent range (normals down to 2^-126,
+// subnormals in steps of 2^-133); magnitudes that round past the largest finite value give inf.
+double round_to_bf16(double v) {
+  if (v == 0.0 || !std::isfinite(v)) return v;
+  int e;
+  std::frexp(v, &e);                        // |v| = m * 2^e, m in [0.5, 1)
+  const int lsb_exp = std::max(e - 8, -133);   // exponent of one unit in the last place
+  const double q = std::nearbyint(std::ldexp(v, -lsb_exp));   // default mode: nearest, ties even
+  const double r = std::ldexp(q, lsb_exp);
+  return std::fabs(r) > 3.3895313892515355e38 ? std::copysign(INFINITY, v) : r;
+}
+
+// RMSNorm.forward on one 512-wide row, before its final cast. The excerpt fixes this step's
+// precision: x = x.float() makes every operation fp32. So: the mean of squares in fp32 (summed in
+// ascending feature order; each square of a bf16 value is exact in fp32), var + eps in fp32,
+// rsqrt as 1 / sqrt with IEEE-rounded fp32 sqrt and division, then x * r and weight * x in fp32.
+void kv_norm_row_precast(const uint16_t* x_bits, const float* gamma, float* y) {
+  float x[kLatent];
+  float sum_sq = 0.0f;
   for (int c = 0; c < kLatent; ++c) {
-    x[c] = bf16_bits_to_double(x_bits[c]);
-    sum_sq += x[c] * x[c];
+    x[c] = static_cast<float>(bf16_bits_to_double(x_bits[c]));
+    sum_sq = sum_sq + x[c] * x[c];
   }
-  const double var = sum_sq / kLatent;
-  const double r = 1.0 / std::sqrt(var + kRmsEps);
-  for (int c = 0; c < kLatent; ++c) y[c] = static_cast<double>(gamma[c]) * (x[c] * r);
+  const float var = sum_sq / static_cast<float>(kLatent);
+  const float r = 1.0f / std::sqrt(var + static_cast<float>(kRmsEps));
+  for (int c = 0; c < kLatent; ++c) y[c] = gamma[c] * (x[c] * r);
+}
+
+// The excerpt ends with `.to(dtype)`: the output goes back to the input's dtype, bf16 for the
+// bf16 latent this path takes.
+void kv_norm_row(const uint16_t* x_bits, const float* gamma, double* y) {
+  float yf[kLatent];
+  kv_norm_row_precast(x_bits, gamma, yf);
+  for (int c = 0; c < kLatent; ++c) y[c] = round_to_bf16(static_cast<double>(yf[c]));
 }
 
 // Canonical selection of query t: the set {j in topk row : 0 <= j <= t}, ascending.
@@ -147,9 +175,24 @@ extern "C" {
 // softmax_scale of MLA __init__ (about 0.13523378).
 double oracle_softmax_scale(void) { return softmax_scale(); }
 
-// kv_norm over N rows of 512: x bf16 bits [N, 512], gamma fp32 [512] -> y fp64 [N, 512].
+// kv_norm over N rows of 512: x bf16 bits [N, 512], gamma fp32 [512] -> y [N, 512] (the values
+// of the bf16 output, as doubles).
 void oracle_kv_norm(const uint16_t* x, const float* gamma, int64_t N, double* y) {
   for (int64_t r = 0; r < N; ++r) kv_norm_row(x + r * kLatent, gamma, y + r * kLatent);
+}
+
+// kv_norm before its final cast to bf16 (the fp32 values, as doubles).
+void oracle_kv_norm_precast(const uint16_t* x, const float* gamma, int64_t N, double* y) {
+  float yf[kLatent];
+  for (int64_t r = 0; r < N; ++r) {
+    kv_norm_row_precast(x + r * kLatent, gamma, yf);
+    for (int c = 0; c < kLatent; ++c) y[r * kLatent + c] = yf[c];
+  }
+}
+
+// The bf16 rounding the kv_norm output goes through, elementwise.
+void oracle_round_to_bf16(const double* x, int64_t n, double* y) {
+  for (int64_t i = 0; i < n; ++i) y[i] = round_to_bf16(x[i]);
 }
 
 // wkv_b up-projection of N normalized rows for all H heads:

@@ -1,0 +1,281 @@
+// libmla: the C ABI (include/mla.h) over the three stages of the MLA sparse prefill.
+// Host code here checks arguments, carves the workspace, encodes the TMA tensor maps and
+// enqueues the kernels on the caller's stream; every step of the path runs in the kernels.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "mla.h"
+#include "ptx.cuh"
+#include "tmap.h"
+#include "canon_select.cuh"
+#include "kvnorm_wkvb.cuh"
+#include "sparse_attn.cuh"
+
+namespace {
+
+constexpr int kLatent = 512, kQK = 192, kRope = 64, kKV = 256;
+constexpr int kMaxT = 65536;
+constexpr int kMaxH = 128;
+constexpr int kMaxDevices = 64;
+
+// Per-device launch set-up: kernel attributes and the SM count, done once per device.
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+mla_status device_setup(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaFuncSetAttribute(mla::k1::kvnorm_wkvb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             mla::k1::SMEM_BYTES) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    if (cudaFuncSetAttribute(mla::k2::sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             mla::k2::SMEM_BYTES) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    d.ready = true;
+  }
+  *num_sms = d.num_sms;
+  return MLA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int bits_words(int T) { return (T + 127) / 128 * 4; }
+
+mla_status check_dims(mla_dims d) {
+  if (d.B < 1 || d.T < 1 || d.H < 1 || d.K < 1) return MLA_ERR_INVALID_ARG;
+  if (d.T > kMaxT || d.H > kMaxH) return MLA_ERR_UNSUPPORTED;
+  const int64_t BT = static_cast<int64_t>(d.B) * d.T;
+  if (BT > INT32_MAX / 2) return MLA_ERR_UNSUPPORTED;
+  const double work = static_cast<double>(BT) * d.H * d.K;
+  if (work >= 1099511627776.0) return MLA_ERR_UNSUPPORTED;  // 2^40
+  return MLA_OK;
+}
+
+size_t kv_bytes(mla_dims d) { return static_cast<size_t>(d.B) * d.H * d.T * kKV * 2; }
+size_t klo_bytes(mla_dims d) { return static_cast<size_t>(d.B) * d.H * d.T * 128; }
+size_t bits_bytes(mla_dims d) { return static_cast<size_t>(d.B) * d.T * bits_words(d.T) * 4; }
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+mla_status launch_canon(const int32_t* topk_idx, mla_dims d, uint32_t* sel_bits, int32_t* n_keys, unsigned flags,
+                        cudaStream_t st) {
+  const int W = bits_words(d.T);
+  const size_t smem = static_cast<size_t>(W) * 4;
+  const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(d.B) * d.T);
+  mla::canon_select_kernel<<<grid, mla::kCanonThreads, smem, st>>>(topk_idx, d.T, d.K, W, sel_bits, n_keys,
+                                                                   (flags & MLA_FLAG_VALIDATE_INDICES) ? 1 : 0);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+mla_status launch_kvnorm_wkvb(const mla_bf16* c_kv, const float* gamma, const mla_bf16* wkv_b, mla_dims d,
+                              uint16_t* kv, uint8_t* klo, int num_sms, cudaStream_t st) {
+  const int M = d.B * d.T;
+  CUtensorMap tm_ckv, tm_w;
+  {
+    const uint64_t dims[2] = {kLatent, static_cast<uint64_t>(M)};
+    const uint64_t strides[1] = {kLatent * 2};
+    const uint32_t box[2] = {64, mla::k1::BM};
+    if (!mla::make_tmap_bf16(&tm_ckv, c_kv, 2, dims, strides, box)) return MLA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[2] = {kLatent, static_cast<uint64_t>(d.H) * kKV};
+    const uint64_t strides[1] = {kLatent * 2};
+    const uint32_t box[2] = {64, mla::k1::BN};
+    if (!mla::make_tmap_bf16(&tm_w, wkv_b, 2, dims, strides, box)) return MLA_ERR_CUDA;
+  }
+  mla::k1::Params p;
+  p.M = M;
+  p.T = d.T;
+  p.H = d.H;
+  p.units = (M + mla::k1::BM - 1) / mla::k1::BM * d.H;
+  p.gamma = gamma;
+  p.kv = kv;
+  p.klo = klo;
+  const int grid = p.units < num_sms ? p.units : num_sms;
+  mla::k1::kvnorm_wkvb_kernel<<<grid, mla::k1::THREADS, mla::k1::SMEM_BYTES, st>>>(tm_ckv, tm_w, p);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+mla_status launch_sparse_attn(const mla_bf16* q, const mla_bf16* k_pe, const uint16_t* kv, const uint8_t* klo,
+                              const uint32_t* sel_bits, mla_bf16* out, float* lse, mla_dims d, cudaStream_t st) {
+  CUtensorMap tm_q, tm_kv, tm_kpe, tm_klo;
+  {
+    const uint64_t dims[4] = {kQK, static_cast<uint64_t>(d.H), static_cast<uint64_t>(d.T), static_cast<uint64_t>(d.B)};
+    const uint64_t strides[3] = {kQK * 2, static_cast<uint64_t>(d.H) * kQK * 2,
+                                 static_cast<uint64_t>(d.T) * d.H * kQK * 2};
+    const uint32_t box[4] = {64, 1, mla::k2::BQ, 1};
+    if (!mla::make_tmap_bf16(&tm_q, q, 4, dims, strides, box)) return MLA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {kKV, static_cast<uint64_t>(d.T), static_cast<uint64_t>(d.B) * d.H};
+    const uint64_t strides[2] = {kKV * 2, static_cast<uint64_t>(d.T) * kKV * 2};
+    const uint32_t box[3] = {64, mla::k2::BK, 1};
+    if (!mla::make_tmap_f16(&tm_kv, kv, 3, dims, strides, box)) return MLA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {kRope, static_cast<uint64_t>(d.T), static_cast<uint64_t>(d.B)};
+    const uint64_t strides[2] = {kRope * 2, static_cast<uint64_t>(d.T) * kRope * 2};
+    const uint32_t box[3] = {64, mla::k2::BK, 1};
+    if (!mla::make_tmap_bf16(&tm_kpe, k_pe, 3, dims, strides, box)) return MLA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {128, static_cast<uint64_t>(d.T), static_cast<uint64_t>(d.B) * d.H};
+    const uint64_t strides[2] = {128, static_cast<uint64_t>(d.T) * 128};
+    const uint32_t box[3] = {128, mla::k2::BK, 1};
+    if (!mla::make_tmap_u8(&tm_klo, klo, 3, dims, strides, box)) return MLA_ERR_CUDA;
+  }
+  mla::k2::Params p;
+  p.B = d.B;
+  p.T = d.T;
+  p.H = d.H;
+  p.nqt = (d.T + mla::k2::BQ - 1) / mla::k2::BQ;
+  p.W = bits_words(d.T);
+  p.scale_log2 = static_cast<float>(mla_softmax_scale() * 1.4426950408889634);
+  p.q = q;
+  p.sel_bits = sel_bits;
+  p.out = out;
+  p.lse = lse;
+  const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(d.B) * d.H * p.nqt);
+  mla::k2::sparse_attn_kernel<<<grid, mla::k2::THREADS, mla::k2::SMEM_BYTES, st>>>(tm_q, tm_kv, tm_kpe, tm_klo, p);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+double mla_softmax_scale(void) {
+  // MLA __init__: qk_head_dim ** -0.5, times mscale^2 (max_seq_len 16384 > original 4096),
+  // mscale = 0.1 * 1 * ln(40) + 1.
+  const double mscale = 0.1 * 1.0 * std::log(40.0) + 1.0;
+  return std::pow(static_cast<double>(kQK), -0.5) * mscale * mscale;
+}
+
+const char* mla_status_string(mla_status s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG: null, misaligned or out-of-range argument";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: shape outside the supported range";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA: a CUDA call or launch failed";
+    case MLA_ERR_INDEX: return "MLA_ERR_INDEX: top-k index outside [0, T)";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a device barrier wait ran out";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: workspace too small or misaligned";
+  }
+  return "unknown mla_status";
+}
+
+size_t mla_sparse_prefill_workspace_size(mla_dims d) {
+  if (check_dims(d) != MLA_OK) return 0;
+  return align_up(kv_bytes(d), 1024) + align_up(klo_bytes(d), 1024) + align_up(bits_bytes(d), 1024);
+}
+
+mla_status mla_canon_select(const int32_t* topk_idx, mla_dims d, uint32_t* sel_bits, int32_t* n_keys,
+                            unsigned flags, void* stream) {
+  mla_status s = check_dims(d);
+  if (s != MLA_OK) return s;
+  if (!topk_idx || !sel_bits || !aligned16(topk_idx) || !aligned16(sel_bits)) return MLA_ERR_INVALID_ARG;
+  if (n_keys && (reinterpret_cast<uintptr_t>(n_keys) & 3u)) return MLA_ERR_INVALID_ARG;
+  int sms;
+  if ((s = device_setup(&sms)) != MLA_OK) return s;
+  return launch_canon(topk_idx, d, sel_bits, n_keys, flags, as_stream(stream));
+}
+
+mla_status mla_kvnorm_wkvb(const mla_bf16* c_kv, const float* gamma, const mla_bf16* wkv_b, mla_dims d,
+                           uint16_t* kv, uint8_t* klo, void* stream) {
+  mla_status s = check_dims(d);
+  if (s != MLA_OK) return s;
+  if (!c_kv || !gamma || !wkv_b || !kv || !klo) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(c_kv) || !aligned16(gamma) || !aligned16(wkv_b) || !aligned16(kv) || !aligned16(klo))
+    return MLA_ERR_INVALID_ARG;
+  int sms;
+  if ((s = device_setup(&sms)) != MLA_OK) return s;
+  return launch_kvnorm_wkvb(c_kv, gamma, wkv_b, d, kv, klo, sms, as_stream(stream));
+}
+
+mla_status mla_sparse_attention(const mla_bf16* q, const mla_bf16* k_pe, const uint16_t* kv, const uint8_t* klo,
+                                const uint32_t* sel_bits, mla_bf16* out, float* lse, mla_dims d, void* stream) {
+  mla_status s = check_dims(d);
+  if (s != MLA_OK) return s;
+  if (!q || !k_pe || !kv || !klo || !sel_bits || !out || !lse) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pe) || !aligned16(kv) || !aligned16(klo) || !aligned16(sel_bits) ||
+      !aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return MLA_ERR_INVALID_ARG;
+  int sms;
+  if ((s = device_setup(&sms)) != MLA_OK) return s;
+  return launch_sparse_attn(q, k_pe, kv, klo, sel_bits, out, lse, d, as_stream(stream));
+}
+
+mla_status mla_sparse_prefill_ex(const mla_bf16* q, const mla_bf16* c_kv, const mla_bf16* k_pe, const float* gamma,
+                                 const mla_bf16* wkv_b, const int32_t* topk_idx, mla_bf16* out, float* lse,
+                                 mla_dims d, void* workspace, size_t workspace_bytes, void* stream,
+                                 int32_t* n_keys, unsigned flags) {
+  mla_status s = check_dims(d);
+  if (s != MLA_OK) return s;
+  if (!q || !c_kv || !k_pe || !gamma || !wkv_b || !topk_idx || !out || !lse) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(c_kv) || !aligned16(k_pe) || !aligned16(gamma) || !aligned16(wkv_b) ||
+      !aligned16(topk_idx) || !aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return MLA_ERR_INVALID_ARG;
+  if (n_keys && (reinterpret_cast<uintptr_t>(n_keys) & 3u)) return MLA_ERR_INVALID_ARG;
+  if (flags & ~MLA_FLAG_VALIDATE_INDICES) return MLA_ERR_INVALID_ARG;
+  const size_t need = mla_sparse_prefill_workspace_size(d);
+  if (workspace != nullptr) {
+    if ((reinterpret_cast<uintptr_t>(workspace) & 1023u) || workspace_bytes < need) return MLA_ERR_WORKSPACE;
+  }
+  int sms;
+  if ((s = device_setup(&sms)) != MLA_OK) return s;
+  cudaStream_t st = as_stream(stream);
+  void* ws = workspace;
+  bool owned = false;
+  if (ws == nullptr) {
+    if (cudaMallocAsync(&ws, need, st) != cudaSuccess) return MLA_ERR_CUDA;
+    owned = true;
+  }
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  uint16_t* kv = reinterpret_cast<uint16_t*>(base);
+  uint8_t* klo = base + align_up(kv_bytes(d), 1024);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(klo + align_up(klo_bytes(d), 1024));
+  s = launch_canon(topk_idx, d, bits, n_keys, flags, st);
+  if (s == MLA_OK) s = launch_kvnorm_wkvb(c_kv, gamma, wkv_b, d, kv, klo, sms, st);
+  if (s == MLA_OK) s = launch_sparse_attn(q, k_pe, kv, klo, bits, out, lse, d, st);
+  if (owned && cudaFreeAsync(ws, st) != cudaSuccess && s == MLA_OK) s = MLA_ERR_CUDA;
+  return s;
+}
+
+mla_status mla_sparse_prefill(const mla_bf16* q, const mla_bf16* c_kv, const mla_bf16* k_pe, const float* gamma,
+                              const mla_bf16* wkv_b, const int32_t* topk_idx, mla_bf16* out, float* lse,
+                              mla_dims d, void* workspace, size_t workspace_bytes, void* stream) {
+  return mla_sparse_prefill_ex(q, c_kv, k_pe, gamma, wkv_b, topk_idx, out, lse, d, workspace, workspace_bytes,
+                               stream, nullptr, 0u);
+}
+
+mla_status mla_get_status(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return MLA_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpyFromSymbol(&word, mla::g_status, sizeof word) != cudaSuccess) return MLA_ERR_CUDA;
+  for (int code = 1; code < 32; ++code)
+    if (word & (1u << code)) return static_cast<mla_status>(code);
+  return MLA_OK;
+}
+
+mla_status mla_clear_status(void) {
+  const unsigned zero = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaMemcpyToSymbol(mla::g_status, &zero, sizeof zero) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,428 @@
+// Stage 4: sparse causal MLA attention (prefill), tcgen05 + TMEM, flash-style online softmax.
+//
+// Per query t and head h ("Keys" / "Scale scores" pages, MHA prefill model.py 574-589):
+//   k_j      = cat(k_nope[j, h], k_pe[j])                       (192 features)
+//   s_j      = softmax_scale * <q[t, h], k_j>,  softmax_scale = 192^-0.5 * (1 + 0.1 ln 40)^2
+//   out[t,h] = sum_{j in S(t)} exp(s_j - M) v[j, h] / sum_{j in S(t)} exp(s_j - M)
+//   lse[t,h] = M + ln sum_{j in S(t)} exp(s_j - M)
+// where S(t) is the canonical selection (top-k as a set, intersected with j <= t) produced by the
+// selection stage as one bitset per query row. The [B, T, T] -inf mask is never built: each
+// softmax thread reads its row's 128-bit slice of the bitset for the key block at hand.
+//
+// One CTA = one (batch, head, 128-query tile). Key blocks of 128 run from 0 to the tile's
+// diagonal block. Per block, the score tile S[128 x 128] (fp32, TMEM, double-buffered) is
+//   q_nope . k_hi   8 UMMAs kind::f16, fp16: A = q_nope from TMEM, B = k_hi from shared memory
+// + q_pe . k_pe     4 UMMAs kind::f16, bf16: both from shared memory (the inputs as given)
+// + q8 . k_lo       4 UMMAs kind::f8f6f4: A = e5m2(q_nope * 2^-11), B = e4m3 residual * 2^11
+// The third term restores the bits of k_nope that fp16 drops, so the scores carry k_nope to about
+// 2^-14 relative (the up-projection stage writes k_hi and k_lo). Then:
+//   softmax: one thread per query row (TMEM lane): scale into the log2 domain, apply the row's
+//           selection bits, running max with lazy rescaling (only when the max grows by more
+//           than 2^8), p = 2^(s - m) rounded to fp16 and written to TMEM (64 cols).
+//   PV    : O[128 x 128] += P[128 x 128] . V[128 x 128], 8 UMMAs kind::f16 with P (fp16) read
+//           from TMEM and V (fp16) from shared memory (MN-major), O in TMEM (128 cols).
+// The MMA issue order QK(i+1), PV(i) lets the softmax of block i+1 overlap the PV of block i.
+//
+// Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-5
+// query preparation, softmax and epilogue (warp w owns TMEM lanes 32*(w%4) .. +31, i.e. 32 rows).
+#pragma once
+
+#include "ptx.cuh"
+
+namespace mla {
+namespace k2 {
+
+constexpr int BQ = 128;                 // queries per tile
+constexpr int BK = 128;                 // keys per block
+constexpr int ATOM_BYTES = 128 * 128;   // 128 rows x 128 bytes, 128-byte swizzle
+constexpr int QPE_BYTES = ATOM_BYTES;   // q[:, 128:192] bf16
+constexpr int Q8_BYTES = ATOM_BYTES;    // e5m2(q[:, 0:128] * 2^-11)
+constexpr int K_BYTES = 4 * ATOM_BYTES;   // k_hi 0-63, k_hi 64-127 (fp16), k_pe (bf16), k_lo (e4m3)
+constexpr int V_BYTES = 2 * ATOM_BYTES;   // v 0-63, 64-127 (fp16)
+constexpr int NK_STAGE = 2;
+constexpr int NV_STAGE = 2;
+constexpr int THREADS = 192;
+constexpr int SMEM_BYTES = QPE_BYTES + Q8_BYTES + NK_STAGE * K_BYTES + NV_STAGE * V_BYTES + 1024;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_S = 0;            // S buffers at cols 0 and 128
+constexpr uint32_t TM_O = 256;          // O at cols 256..383
+constexpr uint32_t TM_QN = 384;         // q_nope as fp16 pairs, cols 384..447
+constexpr uint32_t TM_P = 448;          // P as fp16 pairs, cols 448..511
+constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
+constexpr float Q8_SCALE = 1.0f / 2048.0f; // 2^-11, undoes the 2^11 on k_lo
+
+struct Params {
+  int B, T, H;
+  int nqt;                 // ceil(T / 128)
+  int W;                   // bitset words per query row
+  float scale_log2;        // softmax_scale * log2(e)
+  const uint16_t* q;       // [B, T, H, 192] bf16
+  const uint32_t* sel_bits;
+  uint16_t* out;           // [B, T, H, 128] bf16
+  float* lse;              // [B, T, H]
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    sparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
+                       const __grid_constant__ CUtensorMap tm_kpe, const __grid_constant__ CUtensorMap tm_klo,
+                       const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQpe = smem;
+  uint8_t* sQ8 = sQpe + QPE_BYTES;
+  uint8_t* sK = sQ8 + Q8_BYTES;
+  uint8_t* sV = sK + NK_STAGE * K_BYTES;
+
+  __shared__ uint64_t q_full, q_ready, drain;
+  __shared__ uint64_t k_full[NK_STAGE], k_empty[NK_STAGE];
+  __shared__ uint64_t v_full[NV_STAGE], v_empty[NV_STAGE];
+  __shared__ uint64_t s_full[2], s_free[2], p_full, pv_done[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  volatile int* abort_p = &abort_flag;
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+
+  // work item: heads in order, query tiles of a head from the longest (diagonal-most) down
+  const int item = blockIdx.x;
+  const int bh = item / p.nqt;
+  const int qt = p.nqt - 1 - (item % p.nqt);
+  const int b = bh / p.H, h = bh % p.H;
+  const int t0 = qt * BQ;
+  const int nblk = qt + 1;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&q_full, 1);
+    mbar_init(&q_ready, 128);
+    mbar_init(&drain, 1);
+    for (int s = 0; s < NK_STAGE; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < NV_STAGE; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], 128);
+      mbar_init(&pv_done[s], 1);
+    }
+    mbar_init(&p_full, 128);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kv);
+    tma_prefetch_desc(&tm_kpe);
+    tma_prefetch_desc(&tm_klo);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const int kv_plane = b * p.H + h;
+      bool ok = true;
+      bool kpend[NK_STAGE] = {}, vpend[NV_STAGE] = {};
+      uint32_t kpar[NK_STAGE] = {}, vpar[NV_STAGE] = {};
+      mbar_arrive_expect_tx(&q_full, QPE_BYTES);
+      tma_load_4d(sQpe, &tm_q, &q_full, 128, h, t0, b);
+      int ks = 0, vs = 0;
+      uint32_t kph = 0, vph = 0;
+      // K runs one block ahead of V: K(i+1) never queues behind the wait for a free V stage
+      auto load_k = [&](int i) -> bool {
+        if (!mbar_wait(&k_empty[ks], kph ^ 1, abort_p)) return false;
+        kpend[ks] = false;
+        uint8_t* kdst = sK + ks * K_BYTES;
+        const int j0 = i * BK;
+        mbar_arrive_expect_tx(&k_full[ks], K_BYTES);
+        tma_load_3d(kdst, &tm_kv, &k_full[ks], 0, j0, kv_plane);
+        tma_load_3d(kdst + ATOM_BYTES, &tm_kv, &k_full[ks], 64, j0, kv_plane);
+        tma_load_3d(kdst + 2 * ATOM_BYTES, &tm_kpe, &k_full[ks], 0, j0, b);
+        tma_load_3d(kdst + 3 * ATOM_BYTES, &tm_klo, &k_full[ks], 0, j0, kv_plane);
+        kpend[ks] = true;
+        kpar[ks] = kph;
+        if (++ks == NK_STAGE) { ks = 0; kph ^= 1; }
+        return true;
+      };
+      ok = load_k(0);
+      for (int i = 0; i < nblk && ok; ++i) {
+        if (i + 1 < nblk && !load_k(i + 1)) { ok = false; break; }
+        const int j0 = i * BK;
+        if (!mbar_wait(&v_empty[vs], vph ^ 1, abort_p)) { ok = false; break; }
+        vpend[vs] = false;
+        uint8_t* vdst = sV + vs * V_BYTES;
+        mbar_arrive_expect_tx(&v_full[vs], V_BYTES);
+        tma_load_3d(vdst, &tm_kv, &v_full[vs], 128, j0, kv_plane);
+        tma_load_3d(vdst + ATOM_BYTES, &tm_kv, &v_full[vs], 192, j0, kv_plane);
+        vpend[vs] = true;
+        vpar[vs] = vph;
+        if (++vs == NV_STAGE) { vs = 0; vph ^= 1; }
+      }
+      if (!ok) {
+        // unwinding: let the copies already issued land before shared memory goes away
+        mbar_wait(&q_full, 0, nullptr);
+        for (int s = 0; s < NK_STAGE; ++s)
+          if (kpend[s]) mbar_wait(&k_full[s], kpar[s], nullptr);
+        for (int s = 0; s < NV_STAGE; ++s)
+          if (vpend[s]) mbar_wait(&v_full[s], vpar[s], nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_nope = idesc_f32acc(BQ, BK, kFmtF16, false, false);
+      const uint32_t idesc_rope = idesc_f32acc(BQ, BK, kFmtBF16, false, false);
+      const uint32_t idesc_lo = idesc_f8_f32acc(BQ, BK, kFmtE5M2, kFmtE4M3);
+      const uint32_t idesc_pv = idesc_f32acc(BQ, 128, kFmtF16, false, true);
+      const uint32_t sqpe = smem_u32(sQpe), sq8 = smem_u32(sQ8), sk = smem_u32(sK), sv = smem_u32(sV);
+      bool issued = false;
+      int ks = 0, vs = 0;
+      uint32_t kph = 0, vph = 0;
+      auto issue_qk = [&](int i) -> bool {
+        const int sb = i & 1;
+        // S buffer sb was last read by the softmax of block i-2
+        if (i >= 2 && !mbar_wait(&s_free[sb], ((i - 2) >> 1) & 1, abort_p)) return false;
+        if (!mbar_wait(&k_full[ks], kph, abort_p)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + TM_S + static_cast<uint32_t>(sb * BK);
+        const uint32_t kbase = sk + ks * K_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {   // q_nope (TMEM, fp16) . k_hi
+          const uint64_t bd = sdesc_sw128(kbase + (kk >> 2) * ATOM_BYTES + (kk & 3) * 32, 16, 1024);
+          umma_ts(d, tmem + TM_QN + kk * 8, bd, idesc_nope, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {   // q_pe . k_pe (bf16)
+          const uint64_t ad = sdesc_sw128(sqpe + kk * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(kbase + 2 * ATOM_BYTES + kk * 32, 16, 1024);
+          umma_ss(d, ad, bd, idesc_rope, 1u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {   // e5m2(q_nope 2^-11) . e4m3(k_lo 2^11)
+          const uint64_t ad = sdesc_sw128(sq8 + kk * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(kbase + 3 * ATOM_BYTES + kk * 32, 16, 1024);
+          umma_f8_ss(d, ad, bd, idesc_lo, 1u);
+        }
+        issued = true;
+        umma_commit(&k_empty[ks]);
+        umma_commit(&s_full[sb]);
+        if (++ks == NK_STAGE) { ks = 0; kph ^= 1; }
+        return true;
+      };
+      bool ok = mbar_wait(&q_full, 0, abort_p) && mbar_wait(&q_ready, 0, abort_p);
+      if (ok) ok = issue_qk(0);
+      for (int i = 0; i < nblk && ok; ++i) {
+        if (i + 1 < nblk && !issue_qk(i + 1)) { ok = false; break; }
+        // PV(i): P(i) from TMEM, V(i) from shared memory
+        if (!mbar_wait(&p_full, i & 1, abort_p)) { ok = false; break; }
+        if (!mbar_wait(&v_full[vs], vph, abort_p)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t vbase = sv + vs * V_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bd = sdesc_sw128(vbase + kk * 2048, ATOM_BYTES, 1024);
+          umma_ts(tmem + TM_O, tmem + TM_P + kk * 8, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&v_empty[vs]);
+        umma_commit(&pv_done[i & 1]);   // PV(i) is completion i >> 1 of pv_done[i & 1]
+        if (++vs == NV_STAGE) { vs = 0; vph ^= 1; }
+      }
+      if (issued) {
+        umma_commit(&drain);
+        mbar_wait(&drain, 0, nullptr);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ queries, softmax, epilogue
+    // tcgen05.ld / tcgen05.st are warp-collective: every branch around them is warp-uniform.
+    const int qw = warp & 3;
+    const int r = qw * 32 + lane;           // query row in the tile == TMEM lane
+    const int t = t0 + r;
+    const bool row_valid = t < p.T;
+    const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
+
+    // q_nope of row r: fp16 pairs into TMEM (exact for bf16 values within fp16's range), and
+    // e5m2(q_nope * 2^-11) into the swizzled q8 tile (16-byte chunk c at c ^ (r & 7)).
+    {
+      const uint4* qrow = reinterpret_cast<const uint4*>(
+          p.q + ((static_cast<int64_t>(b) * p.T + (row_valid ? t : 0)) * p.H + h) * 192);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t qn[32];
+        uint32_t q8[16];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = row_valid ? __ldg(qrow + half * 8 + c) : make_uint4(0, 0, 0, 0);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = __uint_as_float(w[e] << 16);
+            const float hi = __uint_as_float(w[e] & 0xFFFF0000u);
+            qn[c * 4 + e] = pack_f16x2(lo, hi);
+            const uint32_t b8 = pack_e5m2x2(lo * Q8_SCALE, hi * Q8_SCALE);
+            if (e & 1)
+              q8[c * 2 + (e >> 1)] |= b8 << 16;
+            else
+              q8[c * 2 + (e >> 1)] = b8;
+          }
+        }
+        tmem_st_32x32b_x32(tmem + lane_off + TM_QN + half * 32, qn);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int chunk = half * 4 + c;   // 16-byte chunk = 16 e5m2 values
+          *reinterpret_cast<uint4*>(sQ8 + r * 128 + ((chunk ^ (r & 7)) * 16)) =
+              make_uint4(q8[c * 4], q8[c * 4 + 1], q8[c * 4 + 2], q8[c * 4 + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&q_ready);
+    }
+
+    const uint32_t* bits_row = p.sel_bits + (static_cast<int64_t>(b) * p.T + (row_valid ? t : 0)) * p.W;
+    float m_ref = -INFINITY;   // running reference max, log2 domain
+    float l = 0.f;             // running sum of the probabilities
+    bool ok = true;
+    uint4 mask_next = row_valid ? __ldg(reinterpret_cast<const uint4*>(bits_row)) : make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < nblk && ok; ++i) {
+      const uint4 mask = mask_next;
+      if (i + 1 < nblk)
+        mask_next = row_valid ? __ldg(reinterpret_cast<const uint4*>(bits_row + (i + 1) * 4)) : make_uint4(0, 0, 0, 0);
+      const int sb = i & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (i >> 1) & 1, abort_p));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t mw[4] = {mask.x, mask.y, mask.z, mask.w};
+      const bool row_any = (mask.x | mask.y | mask.z | mask.w) != 0u;
+      float s[128];
+      if (__any_sync(0xffffffffu, row_any)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + TM_S + static_cast<uint32_t>(sb * BK + c * 32), v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            s[c * 32 + e] = ((mw[c] >> e) & 1u) ? __uint_as_float(v[e]) * p.scale_log2 : -INFINITY;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 128; ++e) s[e] = -INFINITY;
+      }
+      tc_fence_before();
+      mbar_arrive(&s_free[sb]);
+      float mb = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 128; ++e) mb = fmaxf(mb, s[e]);
+      const bool need = mb > m_ref + RESCALE_THRESHOLD;   // true on the first selected key
+      const bool need_o = need && (m_ref != -INFINITY);   // O and l hold earlier blocks' mass
+      const float alpha = need_o ? ex2(m_ref - mb) : 1.0f;
+      if (need_o) l *= alpha;
+      if (need) m_ref = mb;
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;   // no key yet: every p is 0
+      uint32_t pk[64];
+      float lsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float p0 = ex2(s[2 * c] - m_use);
+        const float p1 = ex2(s[2 * c + 1] - m_use);
+        pk[c] = pack_f16x2(p0, p1);
+        lsum += p0 + p1;
+      }
+      l += lsum;
+      if (i > 0) {
+        // P's TMEM columns and O are free once PV(i-1) has completed
+        ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_p));
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, need_o)) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            const uint32_t addr = tmem + lane_off + TM_O + static_cast<uint32_t>(c * 32);
+            tmem_ld_32x32b_x32(addr, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tmem_st_32x32b_x32(addr, v);
+          }
+        }
+      }
+      {
+        uint32_t (&pk0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&pk[0]);
+        uint32_t (&pk1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&pk[32]);
+        tmem_st_32x32b_x32(tmem + lane_off + TM_P, pk0);
+        tmem_st_32x32b_x32(tmem + lane_off + TM_P + 32, pk1);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(nblk - 1) & 1], ((nblk - 1) >> 1) & 1, abort_p));
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = (l > 0.f) ? 1.0f / l : 0.f;
+      uint16_t* orow = p.out + ((static_cast<int64_t>(b) * p.T + (row_valid ? t : 0)) * p.H + h) * 128;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + lane_off + TM_O + static_cast<uint32_t>(c * 32), v);
+        tmem_ld_wait();
+        if (row_valid) {
+          uint4* d4 = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            d4[k] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l),
+                               pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l),
+                               pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l),
+                               pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l));
+          }
+        }
+      }
+      if (row_valid) {
+        const float lse = (l > 0.f) ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        p.lse[(static_cast<int64_t>(b) * p.T + t) * p.H + h] = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace k2
+}  // namespace mla
