@@ -1,0 +1,59 @@
+"""Host-side logic of bench.py (CPU only): the metric's formula, clock-sample parsing and the
+max-over-ranks reduction of a world-size-2 gloo group."""
+
+import os
+import socket
+
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_formula_flops_headline():
+    up, attn = bench.formula_flops(1, 4096, 128, 6292480)
+    assert up == 2 * 4096 * 128 * 512 * 256                      # 137.4 GF
+    assert attn == 2 * 128 * 6292480 * 320                        # 515.5 GF
+    assert abs((up + attn) / 1e9 - 652.9) < 0.1
+
+
+def test_clock_parse():
+    lines = [
+        "0, 1905, 2032, 900.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, 1800, 2032, 1100.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 300, 2032, 100.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "garbage",
+    ]
+    s = bench.ClockSampler.parse(lines)
+    assert s["samples"] == 3 and s["sm_max_mhz"] == 2032
+    assert s["reasons"] == ["sw_power_cap"]
+    assert s["sm_mhz"] in (1800, 1852.5, 1905)                  # median of the loaded samples
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    bench.barrier(dist)
+    q.put((rank, bench.max_over_ranks(1.0 + rank * 2.5, dist)))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = dict(q.get(timeout=10) for _ in range(2))
+    assert got == {0: 3.5, 1: 3.5}
