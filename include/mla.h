@@ -121,6 +121,27 @@ MLA_API mla_status mla_sparse_attention(const mla_bf16* q, const mla_bf16* k_pe,
                                 const uint8_t* klo, const uint32_t* sel_bits, mla_bf16* out, float* lse,
                                 mla_dims d, void* stream);
 
+/* Allocation-free form of mla_sparse_prefill, for callers that cannot allocate device memory
+ * when they run the prefill (code inside an allocator or memory-pool callback, engines that fix
+ * their device footprint ahead of time, hosts that forbid cudaMalloc during a step). The pages
+ * have no counterpart to this: it is a property of this library's interface only.
+ *
+ * Same arguments and results as mla_sparse_prefill, without the workspace: the scratch is a
+ * library-owned device array of MLA_NOALLOC_SCRATCH_BYTES that every GPU loading libmla holds
+ * until the process exits. The call allocates nothing (no cudaMalloc / cudaMallocAsync / cudaFree).
+ *   - Problems whose mla_sparse_prefill_workspace_size(d) exceeds MLA_NOALLOC_SCRATCH_BYTES are
+ *     rejected with MLA_ERR_WORKSPACE before anything is enqueued (at H = 128 that is about 800
+ *     positions in all; the small shapes fit).
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) and
+ *     caches it; make that first call before any stream capture on that device.
+ *   - Every call on a device shares the one array and it keeps the last call's contents (no call
+ *     depends on them). Calls that can overlap on the GPU (other streams, other threads) race on
+ *     it: serialize them. */
+#define MLA_NOALLOC_SCRATCH_BYTES (64u << 20)
+MLA_API mla_status mla_sparse_prefill_noalloc(const mla_bf16* q, const mla_bf16* c_kv, const mla_bf16* k_pe,
+                                              const float* gamma, const mla_bf16* wkv_b, const int32_t* topk_idx,
+                                              mla_bf16* out, float* lse, mla_dims d, void* stream);
+
 /* Device status word of the current device: MLA_OK, or the lowest error code recorded since
  * the last mla_clear_status(). Synchronizes the current device first. */
 MLA_API mla_status mla_get_status(void);

@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
 # every entry point include/mla.h declares
 SYMBOLS = ("mla_sparse_prefill_workspace_size", "mla_sparse_prefill", "mla_sparse_prefill_ex", "mla_canon_select",
            "mla_kvnorm_wkvb", "mla_sparse_attention", "mla_get_status", "mla_clear_status", "mla_softmax_scale",
-           "mla_status_string")
+           "mla_status_string", "mla_sparse_prefill_noalloc")
 
 
 class MlaError(RuntimeError):
@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
         L.mla_softmax_scale.argtypes = []
         L.mla_status_string.restype = ctypes.c_char_p
         L.mla_status_string.argtypes = [I]
+        L.mla_sparse_prefill_noalloc.restype = I
+        L.mla_sparse_prefill_noalloc.argtypes = [P] * 8 + [Dims, P]
         _lib = L
     return _lib
 

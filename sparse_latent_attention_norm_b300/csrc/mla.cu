@@ -262,6 +262,67 @@ mla_status mla_sparse_prefill(const mla_bf16* q, const mla_bf16* c_kv, const mla
                                stream, nullptr, 0u);
 }
 
+// ---------------------------------------------------------------------------------------------
+// Allocation-free variant of mla_sparse_prefill.
+//
+// Some callers cannot allocate device memory at the point where they run the prefill: code
+// running inside a host-side allocator or memory-pool callback, engines that fix their whole
+// device footprint up front, or plug-ins whose host framework forbids cudaMalloc during a step.
+// They get a scratch region that the library owns: a file-scope device array, created when the
+// library's module is loaded on a GPU and kept until the process exits, so every GPU that loads
+// libmla holds these bytes whether or not this entry point is used.
+//
+// Host code cannot pass g_noalloc_scratch to a kernel directly: in host code that name is a
+// host-side stand-in, not a device address. The device address is looked up once per device
+// with cudaGetSymbolAddress (with that device current) on the first call made on that device.
+// ---------------------------------------------------------------------------------------------
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MLA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+void* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mutex;
+
+mla_status noalloc_scratch_address(void** ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return MLA_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return MLA_OK;
+}
+}  // namespace
+
+mla_status mla_sparse_prefill_noalloc(const mla_bf16* q, const mla_bf16* c_kv, const mla_bf16* k_pe,
+                                      const float* gamma, const mla_bf16* wkv_b, const int32_t* topk_idx,
+                                      mla_bf16* out, float* lse, mla_dims d, void* stream) {
+  mla_status s = check_dims(d);
+  if (s != MLA_OK) return s;
+  if (!q || !c_kv || !k_pe || !gamma || !wkv_b || !topk_idx || !out || !lse) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(c_kv) || !aligned16(k_pe) || !aligned16(gamma) || !aligned16(wkv_b) ||
+      !aligned16(topk_idx) || !aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return MLA_ERR_INVALID_ARG;
+  if (mla_sparse_prefill_workspace_size(d) > static_cast<size_t>(MLA_NOALLOC_SCRATCH_BYTES)) return MLA_ERR_WORKSPACE;
+  int sms;
+  if ((s = device_setup(&sms)) != MLA_OK) return s;
+  void* scratch = nullptr;
+  if ((s = noalloc_scratch_address(&scratch)) != MLA_OK) return s;
+  // Same carve as mla_sparse_prefill_ex. Nothing in it has to start at zero: each launch writes
+  // every word the next one reads, so the previous call's leftovers are never used.
+  cudaStream_t st = as_stream(stream);
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  uint16_t* kv = reinterpret_cast<uint16_t*>(base);
+  uint8_t* klo = base + align_up(kv_bytes(d), 1024);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(klo + align_up(klo_bytes(d), 1024));
+  s = launch_canon(topk_idx, d, bits, nullptr, 0u, st);
+  if (s == MLA_OK) s = launch_kvnorm_wkvb(c_kv, gamma, wkv_b, d, kv, klo, sms, st);
+  if (s == MLA_OK) s = launch_sparse_attn(q, k_pe, kv, klo, bits, out, lse, d, st);
+  return s;
+}
+
 mla_status mla_get_status(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return MLA_ERR_CUDA;
   unsigned word = 0;
