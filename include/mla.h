@@ -47,7 +47,8 @@ typedef uint16_t mla_bf16; /* bfloat16 bit pattern */
 typedef enum {
   MLA_OK = 0,
   MLA_ERR_INVALID_ARG = 1, /* null pointer, misalignment, non-positive or overflowing size */
-  MLA_ERR_UNSUPPORTED = 2, /* shape outside what the kernels support (see mla_dims) */
+  MLA_ERR_UNSUPPORTED = 2, /* shape outside what the kernels support (see mla_dims); device: a
+                            * kernel found its shared memory less aligned than its tiles need */
   MLA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
   MLA_ERR_INDEX = 4,       /* device: an index outside [0, T) under MLA_FLAG_VALIDATE_INDICES */
   MLA_ERR_TIMEOUT = 5,     /* device: a barrier wait ran past its limit; the kernel unwound */

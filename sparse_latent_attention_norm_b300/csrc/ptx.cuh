@@ -58,6 +58,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // many nanoseconds gives up, records MLA_ERR_TIMEOUT (code 5) and makes its kernel unwind.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr unsigned kErrTimeout = 5;
+// Recorded when a kernel finds its dynamic shared memory less aligned than its tiles need.
+constexpr unsigned kErrUnsupportedLayout = 2;
 
 // Bounded wait on phase `parity`. Returns false (after recording a timeout) when the limit
 // passes, or at once when `abort_flag` (shared, may be null) is already set by another thread.

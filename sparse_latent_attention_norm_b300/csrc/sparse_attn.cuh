@@ -16,15 +16,20 @@
 // + q8 . k_lo       4 UMMAs kind::f8f6f4: A = e5m2(q_nope * 2^-11), B = e4m3 residual * 2^11
 // The third term restores the bits of k_nope that fp16 drops, so the scores carry k_nope to about
 // 2^-14 relative (the up-projection stage writes k_hi and k_lo). Then:
-//   softmax: one thread per query row (TMEM lane): scale into the log2 domain, apply the row's
-//           selection bits, running max with lazy rescaling (only when the max grows by more
-//           than 2^8), p = 2^(s - m) rounded to fp16 and written to TMEM (64 cols).
+//   softmax: two threads per query row (TMEM lane), 64 key columns each: apply the row's
+//           selection bits, block max of the raw scores (shared between the two threads through
+//           shared memory), running max in the log2 domain with lazy rescaling (only when the
+//           max grows by more than 2^8), p = 2^(s * scale * log2 e - m) rounded to fp16 and
+//           written to TMEM (64 cols of fp16 pairs).
 //   PV    : O[128 x 128] += P[128 x 128] . V[128 x 128], 8 UMMAs kind::f16 with P (fp16) read
 //           from TMEM and V (fp16) from shared memory (MN-major), O in TMEM (128 cols).
-// The MMA issue order QK(i+1), PV(i) lets the softmax of block i+1 overlap the PV of block i.
+// QK^T and PV are issued by two threads, each waiting only on its own barriers, so the scores of
+// blocks i+1 and i+2 are computed while the softmax of block i runs and PV(i) is queued as soon
+// as its probabilities are in TMEM.
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-5
-// query preparation, softmax and epilogue (warp w owns TMEM lanes 32*(w%4) .. +31, i.e. 32 rows).
+// Warp roles (352 threads): warp 0 TMA producer, warp 1 TMEM owner + QK^T MMA issuer, warp 10 PV
+// MMA issuer, warps 2-9 query preparation, softmax and epilogue (warp w owns TMEM lanes
+// 32*(w%4) .. +31, i.e. 32 rows, and key / value columns 64*((w-2)/4) .. +63).
 #pragma once
 
 #include "ptx.cuh"
@@ -41,8 +46,26 @@ constexpr int K_BYTES = 4 * ATOM_BYTES;   // k_hi 0-63, k_hi 64-127 (fp16), k_pe
 constexpr int V_BYTES = 2 * ATOM_BYTES;   // v 0-63, 64-127 (fp16)
 constexpr int NK_STAGE = 2;
 constexpr int NV_STAGE = 2;
-constexpr int THREADS = 192;
-constexpr int SMEM_BYTES = QPE_BYTES + Q8_BYTES + NK_STAGE * K_BYTES + NV_STAGE * V_BYTES + 1024;
+constexpr int THREADS = 352;           // warp 0 TMA, warp 1 QK MMA, warps 2-9 softmax, warp 10 PV MMA
+constexpr int PV_WARP = 10;
+constexpr int NSOFT = 256;             // softmax / epilogue threads
+constexpr int TILE_BYTES = QPE_BYTES + Q8_BYTES + NK_STAGE * K_BYTES + NV_STAGE * V_BYTES;
+
+// Barriers and small shared state, placed after the tiles in the dynamic shared memory (the
+// kernel declares no static shared memory, so the dynamic region starts 1024-byte aligned and
+// needs no alignment slack: the tiles fill all but a few KB of the 227 KB a CTA may use).
+struct Ctrl {
+  float red_max[2][2][BQ];   // [block parity][column half][row]: partial block maxima; after the
+                             // last block, [nblk & 1] holds the partial probability sums
+  uint64_t q_full, q_ready, drain, drain_pv;
+  uint64_t k_full[NK_STAGE], k_empty[NK_STAGE];
+  uint64_t v_full[NV_STAGE], v_empty[NV_STAGE];
+  uint64_t s_full[2], s_free[2], p_full, pv_done[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+constexpr int SMEM_BYTES = TILE_BYTES + static_cast<int>(sizeof(Ctrl));
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;            // S buffers at cols 0 and 128
 constexpr uint32_t TM_O = 256;          // O at cols 256..383
@@ -68,6 +91,24 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// 64-thread named barrier over the two warps of a lane quadrant; returns the AND of `pred` over them.
+__device__ __forceinline__ bool pair_sync_and(int id, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, 64, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -84,19 +125,35 @@ __global__ void __launch_bounds__(THREADS, 1)
     sparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                        const __grid_constant__ CUtensorMap tm_kpe, const __grid_constant__ CUtensorMap tm_klo,
                        const Params p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // The 128-byte swizzle of the tiles needs 1024-byte alignment; the region is only that aligned
+  // when the kernel has no static shared memory, which is checked here once.
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) set_error(kErrUnsupportedLayout);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint8_t* sQpe = smem;
   uint8_t* sQ8 = sQpe + QPE_BYTES;
   uint8_t* sK = sQ8 + Q8_BYTES;
   uint8_t* sV = sK + NK_STAGE * K_BYTES;
 
-  __shared__ uint64_t q_full, q_ready, drain;
-  __shared__ uint64_t k_full[NK_STAGE], k_empty[NK_STAGE];
-  __shared__ uint64_t v_full[NV_STAGE], v_empty[NV_STAGE];
-  __shared__ uint64_t s_full[2], s_free[2], p_full, pv_done[2];
-  __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag;
+  Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem + TILE_BYTES);
+  uint64_t& q_full = ctl.q_full;
+  uint64_t& q_ready = ctl.q_ready;
+  uint64_t& drain = ctl.drain;
+  uint64_t& drain_pv = ctl.drain_pv;
+  uint64_t* k_full = ctl.k_full;
+  uint64_t* k_empty = ctl.k_empty;
+  uint64_t* v_full = ctl.v_full;
+  uint64_t* v_empty = ctl.v_empty;
+  uint64_t* s_full = ctl.s_full;
+  uint64_t* s_free = ctl.s_free;
+  uint64_t& p_full = ctl.p_full;
+  uint64_t* pv_done = ctl.pv_done;
+  uint32_t& tmem_base = ctl.tmem_base;
+  int& abort_flag = ctl.abort_flag;
+  auto& red_max = ctl.red_max;
   volatile int* abort_p = &abort_flag;
 
   const int warp = warp_id();
@@ -113,8 +170,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&q_full, 1);
-    mbar_init(&q_ready, 128);
+    mbar_init(&q_ready, NSOFT);
     mbar_init(&drain, 1);
+    mbar_init(&drain_pv, 1);
     for (int s = 0; s < NK_STAGE; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -125,10 +183,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], 128);
+      mbar_init(&s_free[s], NSOFT);
       mbar_init(&pv_done[s], 1);
     }
-    mbar_init(&p_full, 128);
+    mbar_init(&p_full, NSOFT);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -197,21 +255,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ QK^T MMA issuer
+    // Scores of block i go to S buffer i & 1 once the softmax has read block i-2 out of it.
     if (lane == 0) {
       const uint32_t idesc_nope = idesc_f32acc(BQ, BK, kFmtF16, false, false);
       const uint32_t idesc_rope = idesc_f32acc(BQ, BK, kFmtBF16, false, false);
       const uint32_t idesc_lo = idesc_f8_f32acc(BQ, BK, kFmtE5M2, kFmtE4M3);
-      const uint32_t idesc_pv = idesc_f32acc(BQ, 128, kFmtF16, false, true);
-      const uint32_t sqpe = smem_u32(sQpe), sq8 = smem_u32(sQ8), sk = smem_u32(sK), sv = smem_u32(sV);
+      const uint32_t sqpe = smem_u32(sQpe), sq8 = smem_u32(sQ8), sk = smem_u32(sK);
       bool issued = false;
-      int ks = 0, vs = 0;
-      uint32_t kph = 0, vph = 0;
-      auto issue_qk = [&](int i) -> bool {
+      int ks = 0;
+      uint32_t kph = 0;
+      bool ok = mbar_wait(&q_full, 0, abort_p) && mbar_wait(&q_ready, 0, abort_p);
+      for (int i = 0; i < nblk && ok; ++i) {
         const int sb = i & 1;
-        // S buffer sb was last read by the softmax of block i-2
-        if (i >= 2 && !mbar_wait(&s_free[sb], ((i - 2) >> 1) & 1, abort_p)) return false;
-        if (!mbar_wait(&k_full[ks], kph, abort_p)) return false;
+        if (i >= 2 && !mbar_wait(&s_free[sb], ((i - 2) >> 1) & 1, abort_p)) { ok = false; break; }
+        if (!mbar_wait(&k_full[ks], kph, abort_p)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + TM_S + static_cast<uint32_t>(sb * BK);
         const uint32_t kbase = sk + ks * K_BYTES;
@@ -236,15 +294,28 @@ __global__ void __launch_bounds__(THREADS, 1)
         umma_commit(&k_empty[ks]);
         umma_commit(&s_full[sb]);
         if (++ks == NK_STAGE) { ks = 0; kph ^= 1; }
-        return true;
-      };
-      bool ok = mbar_wait(&q_full, 0, abort_p) && mbar_wait(&q_ready, 0, abort_p);
-      if (ok) ok = issue_qk(0);
-      for (int i = 0; i < nblk && ok; ++i) {
-        if (i + 1 < nblk && !issue_qk(i + 1)) { ok = false; break; }
+      }
+      if (issued) {
+        // every MMA this thread issued has finished before TMEM is released
+        umma_commit(&drain);
+        mbar_wait(&drain, 0, nullptr);
+      }
+    }
+  } else if (warp == PV_WARP) {
+    // ------------------------------------------------------------ PV MMA issuer
+    // A second issuing thread, so that the tensor pipe is fed with the next block's QK^T while
+    // this one waits for the softmax (and the reverse): one thread that waits on both sides
+    // leaves the pipe idle for every wait.
+    if (lane == 0) {
+      const uint32_t idesc_pv = idesc_f32acc(BQ, 128, kFmtF16, false, true);
+      const uint32_t sv = smem_u32(sV);
+      bool issued = false;
+      int vs = 0;
+      uint32_t vph = 0;
+      for (int i = 0; i < nblk; ++i) {
         // PV(i): P(i) from TMEM, V(i) from shared memory
-        if (!mbar_wait(&p_full, i & 1, abort_p)) { ok = false; break; }
-        if (!mbar_wait(&v_full[vs], vph, abort_p)) { ok = false; break; }
+        if (!mbar_wait(&p_full, i & 1, abort_p)) break;
+        if (!mbar_wait(&v_full[vs], vph, abort_p)) break;
         tc_fence_after();
         const uint32_t vbase = sv + vs * V_BYTES;
 #pragma unroll
@@ -252,56 +323,60 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint64_t bd = sdesc_sw128(vbase + kk * 2048, ATOM_BYTES, 1024);
           umma_ts(tmem + TM_O, tmem + TM_P + kk * 8, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
         }
+        issued = true;
         umma_commit(&v_empty[vs]);
         umma_commit(&pv_done[i & 1]);   // PV(i) is completion i >> 1 of pv_done[i & 1]
         if (++vs == NV_STAGE) { vs = 0; vph ^= 1; }
       }
       if (issued) {
-        umma_commit(&drain);
-        mbar_wait(&drain, 0, nullptr);
+        umma_commit(&drain_pv);
+        mbar_wait(&drain_pv, 0, nullptr);
       }
     }
   } else {
     // ------------------------------------------------------------ queries, softmax, epilogue
+    // Two warps per TMEM lane quadrant: warp w (2..9) owns rows 32*(w%4) .. +31 and key columns
+    // 64*half .. +63 of every block, half = (w-2)/4. The pair shares its rows' running max through
+    // shared memory at a 64-thread named barrier (id 1 + quadrant) once per block; that barrier
+    // also ANDs the pair's wait results so both warps of a pair always take the same exit.
     // tcgen05.ld / tcgen05.st are warp-collective: every branch around them is warp-uniform.
     const int qw = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = qw * 32 + lane;           // query row in the tile == TMEM lane
     const int t = t0 + r;
     const bool row_valid = t < p.T;
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
+    const int pair_bar = 1 + qw;
 
-    // q_nope of row r: fp16 pairs into TMEM (exact for bf16 values within fp16's range), and
-    // e5m2(q_nope * 2^-11) into the swizzled q8 tile (16-byte chunk c at c ^ (r & 7)).
+    // q_nope[64*half .. +63] of row r: fp16 pairs into TMEM (exact for bf16 values within fp16's
+    // range), and e5m2(q_nope * 2^-11) into the swizzled q8 tile (16-byte chunk c at c ^ (r & 7)).
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(
           p.q + ((static_cast<int64_t>(b) * p.T + (row_valid ? t : 0)) * p.H + h) * 192);
+      uint32_t qn[32];
+      uint32_t q8[16];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t qn[32];
-        uint32_t q8[16];
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = row_valid ? __ldg(qrow + half * 8 + c) : make_uint4(0, 0, 0, 0);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = row_valid ? __ldg(qrow + half * 8 + c) : make_uint4(0, 0, 0, 0);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float lo = __uint_as_float(w[e] << 16);
-            const float hi = __uint_as_float(w[e] & 0xFFFF0000u);
-            qn[c * 4 + e] = pack_f16x2(lo, hi);
-            const uint32_t b8 = pack_e5m2x2(lo * Q8_SCALE, hi * Q8_SCALE);
-            if (e & 1)
-              q8[c * 2 + (e >> 1)] |= b8 << 16;
-            else
-              q8[c * 2 + (e >> 1)] = b8;
-          }
+        for (int e = 0; e < 4; ++e) {
+          const float lo = __uint_as_float(w[e] << 16);
+          const float hi = __uint_as_float(w[e] & 0xFFFF0000u);
+          qn[c * 4 + e] = pack_f16x2(lo, hi);
+          const uint32_t b8 = pack_e5m2x2(lo * Q8_SCALE, hi * Q8_SCALE);
+          if (e & 1)
+            q8[c * 2 + (e >> 1)] |= b8 << 16;
+          else
+            q8[c * 2 + (e >> 1)] = b8;
         }
-        tmem_st_32x32b_x32(tmem + lane_off + TM_QN + half * 32, qn);
+      }
+      tmem_st_32x32b_x32(tmem + lane_off + TM_QN + half * 32, qn);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int chunk = half * 4 + c;   // 16-byte chunk = 16 e5m2 values
-          *reinterpret_cast<uint4*>(sQ8 + r * 128 + ((chunk ^ (r & 7)) * 16)) =
-              make_uint4(q8[c * 4], q8[c * 4 + 1], q8[c * 4 + 2], q8[c * 4 + 3]);
-        }
+      for (int c = 0; c < 4; ++c) {
+        const int chunk = half * 4 + c;   // 16-byte chunk = 16 e5m2 values
+        *reinterpret_cast<uint4*>(sQ8 + r * 128 + ((chunk ^ (r & 7)) * 16)) =
+            make_uint4(q8[c * 4], q8[c * 4 + 1], q8[c * 4 + 2], q8[c * 4 + 3]);
       }
       tmem_st_wait();
       fence_proxy_async_smem();
@@ -309,67 +384,85 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive(&q_ready);
     }
 
-    const uint32_t* bits_row = p.sel_bits + (static_cast<int64_t>(b) * p.T + (row_valid ? t : 0)) * p.W;
-    float m_ref = -INFINITY;   // running reference max, log2 domain
-    float l = 0.f;             // running sum of the probabilities
+    // this thread's two selection words of block i: keys 64*half .. +63 of the block
+    const uint2* bits_row = reinterpret_cast<const uint2*>(
+        p.sel_bits + (static_cast<int64_t>(b) * p.T + (row_valid ? t : 0)) * p.W) + half;
+    const float sl2 = p.scale_log2;
+    float m_ref = -INFINITY;   // running reference max, log2 domain (identical in both warps of a pair)
+    float l = 0.f;             // running sum of this thread's 64 columns' probabilities
     bool ok = true;
-    uint4 mask_next = row_valid ? __ldg(reinterpret_cast<const uint4*>(bits_row)) : make_uint4(0, 0, 0, 0);
-    for (int i = 0; i < nblk && ok; ++i) {
-      const uint4 mask = mask_next;
-      if (i + 1 < nblk)
-        mask_next = row_valid ? __ldg(reinterpret_cast<const uint4*>(bits_row + (i + 1) * 4)) : make_uint4(0, 0, 0, 0);
+    uint2 mask_next = row_valid ? __ldg(bits_row) : make_uint2(0, 0);
+    for (int i = 0; i < nblk; ++i) {
+      const uint2 mask = mask_next;
+      if (i + 1 < nblk) mask_next = row_valid ? __ldg(bits_row + (i + 1) * 2) : make_uint2(0, 0);
       const int sb = i & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (i >> 1) & 1, abort_p));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t mw[4] = {mask.x, mask.y, mask.z, mask.w};
-      const bool row_any = (mask.x | mask.y | mask.z | mask.w) != 0u;
-      float s[128];
-      if (__any_sync(0xffffffffu, row_any)) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + TM_S + static_cast<uint32_t>(sb * BK + c * 32), v);
+      bool got = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (i >> 1) & 1, abort_p));
+      float s[64];
+      if (got) {
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, (mask.x | mask.y) != 0u)) {
+          uint32_t v[64];
+          const uint32_t sa = tmem + lane_off + TM_S + static_cast<uint32_t>(sb * BK + half * 64);
+          tmem_ld_32x32b_x32(sa, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld_32x32b_x32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            s[c * 32 + e] = ((mw[c] >> e) & 1u) ? __uint_as_float(v[e]) * p.scale_log2 : -INFINITY;
+          for (int e = 0; e < 32; ++e) {
+            s[e] = ((mask.x >> e) & 1u) ? __uint_as_float(v[e]) : -INFINITY;
+            s[32 + e] = ((mask.y >> e) & 1u) ? __uint_as_float(v[32 + e]) : -INFINITY;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) s[e] = -INFINITY;
         }
+        tc_fence_before();
+        mbar_arrive(&s_free[sb]);
       } else {
 #pragma unroll
-        for (int e = 0; e < 128; ++e) s[e] = -INFINITY;
+        for (int e = 0; e < 64; ++e) s[e] = -INFINITY;
       }
-      tc_fence_before();
-      mbar_arrive(&s_free[sb]);
-      float mb = -INFINITY;
+      // raw (unscaled) block max of the selected scores; the scale is positive, so scaling
+      // the max gives the max of the scaled scores exactly
+      float mx[4];   // four independent chains: mx[k] covers columns congruent to k mod 4
 #pragma unroll
-      for (int e = 0; e < 128; ++e) mb = fmaxf(mb, s[e]);
+      for (int k = 0; k < 4; ++k) mx[k] = fmaxf(s[k], s[4 + k]);
+#pragma unroll
+      for (int e = 8; e < 64; e += 8)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mx[k] = max3f(mx[k], s[e + k], s[e + 4 + k]);
+      const float mloc = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+      red_max[sb][half][r] = mloc;
+      ok = pair_sync_and(pair_bar, ok && got);
+      if (!ok) break;
+      const float mb = fmaxf(mloc, red_max[sb][half ^ 1][r]) * sl2;
       const bool need = mb > m_ref + RESCALE_THRESHOLD;   // true on the first selected key
       const bool need_o = need && (m_ref != -INFINITY);   // O and l hold earlier blocks' mass
       const float alpha = need_o ? ex2(m_ref - mb) : 1.0f;
       if (need_o) l *= alpha;
       if (need) m_ref = mb;
-      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;   // no key yet: every p is 0
-      uint32_t pk[64];
-      float lsum = 0.f;
+      const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;   // no key yet: every p is 0
+      uint32_t pk[32];
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2(s[2 * c] - m_use);
-        const float p1 = ex2(s[2 * c + 1] - m_use);
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ex2(fmaf(s[2 * c], sl2, neg_m));
+        const float p1 = ex2(fmaf(s[2 * c + 1], sl2, neg_m));
         pk[c] = pack_f16x2(p0, p1);
-        lsum += p0 + p1;
+        ls[c & 3] += p0 + p1;
       }
-      l += lsum;
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       if (i > 0) {
-        // P's TMEM columns and O are free once PV(i-1) has completed
-        ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_p));
-        if (!ok) break;
+        // P's TMEM columns and O are free once PV(i-1) has completed. A failed wait here is
+        // carried into the next block's pair barrier (or the epilogue's), so both warps of the
+        // pair leave together; the writes below then only touch this CTA's own TMEM.
+        const bool pv_ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_p));
+        ok = ok && pv_ok;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, need_o)) {
+        if (pv_ok && __any_sync(0xffffffffu, need_o)) {
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t v[32];
-            const uint32_t addr = tmem + lane_off + TM_O + static_cast<uint32_t>(c * 32);
+            const uint32_t addr = tmem + lane_off + TM_O + static_cast<uint32_t>(half * 64 + c * 32);
             tmem_ld_32x32b_x32(addr, v);
             tmem_ld_wait();
 #pragma unroll
@@ -378,25 +471,25 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      {
-        uint32_t (&pk0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&pk[0]);
-        uint32_t (&pk1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&pk[32]);
-        tmem_st_32x32b_x32(tmem + lane_off + TM_P, pk0);
-        tmem_st_32x32b_x32(tmem + lane_off + TM_P + 32, pk1);
-      }
+      tmem_st_32x32b_x32(tmem + lane_off + TM_P + half * 32, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full);
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(nblk - 1) & 1], ((nblk - 1) >> 1) & 1, abort_p));
+    // partial sums go to the parity the last block did not use (its reads finished before the
+    // last block's pair barrier)
+    red_max[nblk & 1][half][r] = l;
+    ok = pair_sync_and(pair_bar, ok);
     if (ok) {
       tc_fence_after();
-      const float inv_l = (l > 0.f) ? 1.0f / l : 0.f;
-      uint16_t* orow = p.out + ((static_cast<int64_t>(b) * p.T + (row_valid ? t : 0)) * p.H + h) * 128;
+      const float lt = l + red_max[nblk & 1][half ^ 1][r];
+      const float inv_l = (lt > 0.f) ? 1.0f / lt : 0.f;
+      uint16_t* orow = p.out + ((static_cast<int64_t>(b) * p.T + (row_valid ? t : 0)) * p.H + h) * 128 + half * 64;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + TM_O + static_cast<uint32_t>(c * 32), v);
+        tmem_ld_32x32b_x32(tmem + lane_off + TM_O + static_cast<uint32_t>(half * 64 + c * 32), v);
         tmem_ld_wait();
         if (row_valid) {
           uint4* d4 = reinterpret_cast<uint4*>(orow + c * 32);
@@ -409,8 +502,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      if (row_valid) {
-        const float lse = (l > 0.f) ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
+      if (row_valid && half == 0) {
+        const float lse = (lt > 0.f) ? (m_ref + log2f(lt)) * 0.6931471805599453f : -INFINITY;
         p.lse[(static_cast<int64_t>(b) * p.T + t) * p.H + h] = lse;
       }
     }
