@@ -16,20 +16,20 @@
 // + q8 . k_lo       4 UMMAs kind::f8f6f4: A = e5m2(q_nope * 2^-11), B = e4m3 residual * 2^11
 // The third term restores the bits of k_nope that fp16 drops, so the scores carry k_nope to about
 // 2^-14 relative (the up-projection stage writes k_hi and k_lo). Then:
-//   softmax: two threads per query row (TMEM lane), 64 key columns each: apply the row's
-//           selection bits, block max of the raw scores (shared between the two threads through
-//           shared memory), running max in the log2 domain with lazy rescaling (only when the
-//           max grows by more than 2^8), p = 2^(s * scale * log2 e - m) rounded to fp16 and
-//           written to TMEM (64 cols of fp16 pairs).
+//   softmax: four threads per query row (TMEM lane), 32 key columns each: apply the row's
+//           selection bits, block max of the raw scores (combined across the four threads with
+//           shared atomicMax), running max in the log2 domain with lazy rescaling (only when the
+//           max grows by more than 2^8), p = 2^(s * scale * log2 e - m) evaluated in fp16
+//           (ex2.approx.f16x2) and written to TMEM (64 cols of fp16 pairs).
 //   PV    : O[128 x 128] += P[128 x 128] . V[128 x 128], 8 UMMAs kind::f16 with P (fp16) read
 //           from TMEM and V (fp16) from shared memory (MN-major), O in TMEM (128 cols).
 // QK^T and PV are issued by two threads, each waiting only on its own barriers, so the scores of
 // blocks i+1 and i+2 are computed while the softmax of block i runs and PV(i) is queued as soon
 // as its probabilities are in TMEM.
 //
-// Warp roles (352 threads): warp 0 TMA producer, warp 1 TMEM owner + QK^T MMA issuer, warp 10 PV
-// MMA issuer, warps 2-9 query preparation, softmax and epilogue (warp w owns TMEM lanes
-// 32*(w%4) .. +31, i.e. 32 rows, and key / value columns 64*((w-2)/4) .. +63).
+// Warp roles (608 threads): warp 0 TMA producer, warp 1 TMEM owner + QK^T MMA issuer, warp 18 PV
+// MMA issuer, warps 2-17 query preparation, softmax and epilogue (warp w owns TMEM lanes
+// 32*(w%4) .. +31, i.e. 32 rows, and key / value columns 32*((w-2)/4) .. +31).
 #pragma once
 
 #include "ptx.cuh"
@@ -46,17 +46,19 @@ constexpr int K_BYTES = 4 * ATOM_BYTES;   // k_hi 0-63, k_hi 64-127 (fp16), k_pe
 constexpr int V_BYTES = 2 * ATOM_BYTES;   // v 0-63, 64-127 (fp16)
 constexpr int NK_STAGE = 2;
 constexpr int NV_STAGE = 2;
-constexpr int THREADS = 352;           // warp 0 TMA, warp 1 QK MMA, warps 2-9 softmax, warp 10 PV MMA
-constexpr int PV_WARP = 10;
-constexpr int NSOFT = 256;             // softmax / epilogue threads
+constexpr int NPART = 4;                // softmax warps per TMEM lane quadrant (column parts)
+constexpr int PCOLS = BK / NPART;       // key / value columns per softmax thread
+constexpr int NSOFT = 128 * NPART;      // softmax / epilogue threads
+constexpr int PV_WARP = 2 + NSOFT / 32; // warp 0 TMA, warp 1 QK MMA, warps 2.. softmax, then PV MMA
+constexpr int THREADS = 32 * (PV_WARP + 1);
 constexpr int TILE_BYTES = QPE_BYTES + Q8_BYTES + NK_STAGE * K_BYTES + NV_STAGE * V_BYTES;
 
 // Barriers and small shared state, placed after the tiles in the dynamic shared memory (the
 // kernel declares no static shared memory, so the dynamic region starts 1024-byte aligned and
 // needs no alignment slack: the tiles fill all but a few KB of the 227 KB a CTA may use).
 struct Ctrl {
-  float red_max[2][2][BQ];   // [block parity][column half][row]: partial block maxima; after the
-                             // last block, [nblk & 1] holds the partial probability sums
+  int max_key[3][BQ];        // [block % 3][row]: block max of the row's selected raw scores, as an
+                             // order-preserving integer key, reduced with shared atomicMax
   uint64_t q_full, q_ready, drain, drain_pv;
   uint64_t k_full[NK_STAGE], k_empty[NK_STAGE];
   uint64_t v_full[NV_STAGE], v_empty[NV_STAGE];
@@ -91,22 +93,47 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// 2^x for the two fp16 halves of `x` (low half first), fp16 results in the same places.
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// acc + lo(h) + hi(h): both fp16 halves of `h` added to an fp32 accumulator in fp32.
+__device__ __forceinline__ float add_f16x2_to_f32(uint32_t h, float acc) {
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+      "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %0, hi, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(h));
+  return acc;
+}
+
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
 
-// 64-thread named barrier over the two warps of a lane quadrant; returns the AND of `pred` over them.
-__device__ __forceinline__ bool pair_sync_and(int id, bool pred) {
+// Named barrier over the NPART softmax warps of a lane quadrant; returns the AND of `pred` over them.
+__device__ __forceinline__ bool quad_sync_and(int id, bool pred) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, 64, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred)), "r"(id)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "n"(32 * NPART)
       : "memory");
   return r != 0;
+}
+
+// Order-preserving map from non-NaN floats to ints (a < b iff key(a) < key(b)) and its inverse.
+__device__ __forceinline__ int float_order_key(float f) {
+  const int i = __float_as_int(f);
+  return i >= 0 ? i : (i ^ 0x7FFFFFFF);
+}
+__device__ __forceinline__ float float_from_order_key(int k) {
+  return __int_as_float(k >= 0 ? k : (k ^ 0x7FFFFFFF));
 }
 
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -153,7 +180,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* pv_done = ctl.pv_done;
   uint32_t& tmem_base = ctl.tmem_base;
   int& abort_flag = ctl.abort_flag;
-  auto& red_max = ctl.red_max;
+  auto& max_key = ctl.max_key;
   volatile int* abort_p = &abort_flag;
 
   const int warp = warp_id();
@@ -167,6 +194,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int t0 = qt * BQ;
   const int nblk = qt + 1;
 
+  for (int i = threadIdx.x; i < 3 * BQ; i += THREADS) (&max_key[0][0])[i] = INT_MIN;
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&q_full, 1);
@@ -261,7 +289,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t idesc_nope = idesc_f32acc(BQ, BK, kFmtF16, false, false);
       const uint32_t idesc_rope = idesc_f32acc(BQ, BK, kFmtBF16, false, false);
       const uint32_t idesc_lo = idesc_f8_f32acc(BQ, BK, kFmtE5M2, kFmtE4M3);
-      const uint32_t sqpe = smem_u32(sQpe), sq8 = smem_u32(sQ8), sk = smem_u32(sK);
+      // Descriptors of every operand tile, computed once: the start-address field is bits 0-13
+      // (address >> 4) and no offset used below carries out of it (shared memory < 256 KB),
+      // so the descriptor of (tile + offset) is the tile's descriptor + (offset >> 4).
+      static_assert(NK_STAGE == 2 && NV_STAGE == 2, "stage descriptors below");
+      const uint64_t d_k0 = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t d_k1 = sdesc_sw128(smem_u32(sK + K_BYTES), 16, 1024);
+      const uint64_t d_qpe = sdesc_sw128(smem_u32(sQpe), 16, 1024);
+      const uint64_t d_q8 = sdesc_sw128(smem_u32(sQ8), 16, 1024);
       bool issued = false;
       int ks = 0;
       uint32_t kph = 0;
@@ -272,24 +307,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait(&k_full[ks], kph, abort_p)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + TM_S + static_cast<uint32_t>(sb * BK);
-        const uint32_t kbase = sk + ks * K_BYTES;
+        const uint64_t dk = ks ? d_k1 : d_k0;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {   // q_nope (TMEM, fp16) . k_hi
-          const uint64_t bd = sdesc_sw128(kbase + (kk >> 2) * ATOM_BYTES + (kk & 3) * 32, 16, 1024);
-          umma_ts(d, tmem + TM_QN + kk * 8, bd, idesc_nope, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk)   // q_nope (TMEM, fp16) . k_hi
+          umma_ts(d, tmem + TM_QN + kk * 8, dk + (((kk >> 2) * ATOM_BYTES + (kk & 3) * 32) >> 4), idesc_nope,
+                  kk > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {   // q_pe . k_pe (bf16)
-          const uint64_t ad = sdesc_sw128(sqpe + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(kbase + 2 * ATOM_BYTES + kk * 32, 16, 1024);
-          umma_ss(d, ad, bd, idesc_rope, 1u);
-        }
+        for (int kk = 0; kk < 4; ++kk)   // q_pe . k_pe (bf16)
+          umma_ss(d, d_qpe + kk * 2, dk + ((2 * ATOM_BYTES + kk * 32) >> 4), idesc_rope, 1u);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {   // e5m2(q_nope 2^-11) . e4m3(k_lo 2^11)
-          const uint64_t ad = sdesc_sw128(sq8 + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(kbase + 3 * ATOM_BYTES + kk * 32, 16, 1024);
-          umma_f8_ss(d, ad, bd, idesc_lo, 1u);
-        }
+        for (int kk = 0; kk < 4; ++kk)   // e5m2(q_nope 2^-11) . e4m3(k_lo 2^11)
+          umma_f8_ss(d, d_q8 + kk * 2, dk + ((3 * ATOM_BYTES + kk * 32) >> 4), idesc_lo, 1u);
         issued = true;
         umma_commit(&k_empty[ks]);
         umma_commit(&s_full[sb]);
@@ -308,7 +336,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // leaves the pipe idle for every wait.
     if (lane == 0) {
       const uint32_t idesc_pv = idesc_f32acc(BQ, 128, kFmtF16, false, true);
-      const uint32_t sv = smem_u32(sV);
+      const uint64_t d_v0 = sdesc_sw128(smem_u32(sV), ATOM_BYTES, 1024);
+      const uint64_t d_v1 = sdesc_sw128(smem_u32(sV + V_BYTES), ATOM_BYTES, 1024);
       bool issued = false;
       int vs = 0;
       uint32_t vph = 0;
@@ -317,12 +346,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait(&p_full, i & 1, abort_p)) break;
         if (!mbar_wait(&v_full[vs], vph, abort_p)) break;
         tc_fence_after();
-        const uint32_t vbase = sv + vs * V_BYTES;
+        const uint64_t dv = vs ? d_v1 : d_v0;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bd = sdesc_sw128(vbase + kk * 2048, ATOM_BYTES, 1024);
-          umma_ts(tmem + TM_O, tmem + TM_P + kk * 8, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk)   // 16 keys per UMMA: 16 rows of 128 bytes = 2048 bytes
+          umma_ts(tmem + TM_O, tmem + TM_P + kk * 8, dv + ((kk * 2048) >> 4), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
         issued = true;
         umma_commit(&v_empty[vs]);
         umma_commit(&pv_done[i & 1]);   // PV(i) is completion i >> 1 of pv_done[i & 1]
@@ -335,29 +362,30 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ queries, softmax, epilogue
-    // Two warps per TMEM lane quadrant: warp w (2..9) owns rows 32*(w%4) .. +31 and key columns
-    // 64*half .. +63 of every block, half = (w-2)/4. The pair shares its rows' running max through
-    // shared memory at a 64-thread named barrier (id 1 + quadrant) once per block; that barrier
-    // also ANDs the pair's wait results so both warps of a pair always take the same exit.
+    // NPART warps per TMEM lane quadrant: warp w owns rows 32*(w%4) .. +31 and key / value
+    // columns PCOLS*part .. +PCOLS-1 of every block, part = (w-2)/4. The quadrant's warps combine
+    // their rows' block maxima with shared atomicMax on order-preserving integer keys and meet
+    // once per block at a named barrier (id 1 + quadrant) that also ANDs their wait results, so
+    // all of them take the same exit.
     // tcgen05.ld / tcgen05.st are warp-collective: every branch around them is warp-uniform.
     const int qw = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int part = (warp - 2) >> 2;
     const int r = qw * 32 + lane;           // query row in the tile == TMEM lane
     const int t = t0 + r;
     const bool row_valid = t < p.T;
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
-    const int pair_bar = 1 + qw;
+    const int quad_bar = 1 + qw;
 
-    // q_nope[64*half .. +63] of row r: fp16 pairs into TMEM (exact for bf16 values within fp16's
+    // q_nope[32*part .. +31] of row r: fp16 pairs into TMEM (exact for bf16 values within fp16's
     // range), and e5m2(q_nope * 2^-11) into the swizzled q8 tile (16-byte chunk c at c ^ (r & 7)).
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(
           p.q + ((static_cast<int64_t>(b) * p.T + (row_valid ? t : 0)) * p.H + h) * 192);
-      uint32_t qn[32];
-      uint32_t q8[16];
+      uint32_t qn[16];
+      uint32_t q8[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 v = row_valid ? __ldg(qrow + half * 8 + c) : make_uint4(0, 0, 0, 0);
+      for (int c = 0; c < 4; ++c) {
+        const uint4 v = row_valid ? __ldg(qrow + part * 4 + c) : make_uint4(0, 0, 0, 0);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -371,10 +399,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             q8[c * 2 + (e >> 1)] = b8;
         }
       }
-      tmem_st_32x32b_x32(tmem + lane_off + TM_QN + half * 32, qn);
+      tmem_st_32x32b_x16(tmem + lane_off + TM_QN + part * 16, qn);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int chunk = half * 4 + c;   // 16-byte chunk = 16 e5m2 values
+      for (int c = 0; c < 2; ++c) {
+        const int chunk = part * 2 + c;   // 16-byte chunk = 16 e5m2 values
         *reinterpret_cast<uint4*>(sQ8 + r * 128 + ((chunk ^ (r & 7)) * 16)) =
             make_uint4(q8[c * 4], q8[c * 4 + 1], q8[c * 4 + 2], q8[c * 4 + 3]);
       }
@@ -384,42 +412,38 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive(&q_ready);
     }
 
-    // this thread's two selection words of block i: keys 64*half .. +63 of the block
-    const uint2* bits_row = reinterpret_cast<const uint2*>(
-        p.sel_bits + (static_cast<int64_t>(b) * p.T + (row_valid ? t : 0)) * p.W) + half;
+    // this thread's selection word of block i: keys PCOLS*part .. +31 of the block
+    const uint32_t* bits_row =
+        p.sel_bits + (static_cast<int64_t>(b) * p.T + (row_valid ? t : 0)) * p.W + part;
     const float sl2 = p.scale_log2;
-    float m_ref = -INFINITY;   // running reference max, log2 domain (identical in both warps of a pair)
-    float l = 0.f;             // running sum of this thread's 64 columns' probabilities
+    float m_ref = -INFINITY;   // running reference max, log2 domain (identical in the quadrant's warps)
+    float l = 0.f;             // running sum of this thread's columns' probabilities
     bool ok = true;
-    uint2 mask_next = row_valid ? __ldg(bits_row) : make_uint2(0, 0);
+    uint32_t mask_next = row_valid ? __ldg(bits_row) : 0u;
     for (int i = 0; i < nblk; ++i) {
-      const uint2 mask = mask_next;
-      if (i + 1 < nblk) mask_next = row_valid ? __ldg(bits_row + (i + 1) * 2) : make_uint2(0, 0);
+      const uint32_t mask = mask_next;
+      if (i + 1 < nblk) mask_next = row_valid ? __ldg(bits_row + (i + 1) * 4) : 0u;
       const int sb = i & 1;
+      const int slot = i % 3;
       bool got = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (i >> 1) & 1, abort_p));
-      float s[64];
+      float s[PCOLS];
       if (got) {
         tc_fence_after();
-        if (__any_sync(0xffffffffu, (mask.x | mask.y) != 0u)) {
-          uint32_t v[64];
-          const uint32_t sa = tmem + lane_off + TM_S + static_cast<uint32_t>(sb * BK + half * 64);
-          tmem_ld_32x32b_x32(sa, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-          tmem_ld_32x32b_x32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        if (__any_sync(0xffffffffu, mask != 0u)) {
+          uint32_t v[PCOLS];
+          tmem_ld_32x32b_x32(tmem + lane_off + TM_S + static_cast<uint32_t>(sb * BK + part * PCOLS), v);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            s[e] = ((mask.x >> e) & 1u) ? __uint_as_float(v[e]) : -INFINITY;
-            s[32 + e] = ((mask.y >> e) & 1u) ? __uint_as_float(v[32 + e]) : -INFINITY;
-          }
+          for (int e = 0; e < PCOLS; ++e) s[e] = ((mask >> e) & 1u) ? __uint_as_float(v[e]) : -INFINITY;
         } else {
 #pragma unroll
-          for (int e = 0; e < 64; ++e) s[e] = -INFINITY;
+          for (int e = 0; e < PCOLS; ++e) s[e] = -INFINITY;
         }
         tc_fence_before();
         mbar_arrive(&s_free[sb]);
       } else {
 #pragma unroll
-        for (int e = 0; e < 64; ++e) s[e] = -INFINITY;
+        for (int e = 0; e < PCOLS; ++e) s[e] = -INFINITY;
       }
       // raw (unscaled) block max of the selected scores; the scale is positive, so scaling
       // the max gives the max of the scaled scores exactly
@@ -427,84 +451,84 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int k = 0; k < 4; ++k) mx[k] = fmaxf(s[k], s[4 + k]);
 #pragma unroll
-      for (int e = 8; e < 64; e += 8)
+      for (int e = 8; e < PCOLS; e += 8)
 #pragma unroll
         for (int k = 0; k < 4; ++k) mx[k] = max3f(mx[k], s[e + k], s[e + 4 + k]);
-      const float mloc = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3]));
-      red_max[sb][half][r] = mloc;
-      ok = pair_sync_and(pair_bar, ok && got);
+      atomicMax(&max_key[slot][r], float_order_key(max3f(mx[0], mx[1], fmaxf(mx[2], mx[3]))));
+      ok = quad_sync_and(quad_bar, ok && got);
       if (!ok) break;
-      const float mb = fmaxf(mloc, red_max[sb][half ^ 1][r]) * sl2;
+      const float mb = float_from_order_key(max_key[slot][r]) * sl2;
+      // the slot of block i-1 has been read by every warp of the quadrant (each read it before
+      // arriving at this block's barrier); it is next written at block i+2, after the next barrier
+      if (part == 0 && i > 0) max_key[(i + 2) % 3][r] = INT_MIN;
       const bool need = mb > m_ref + RESCALE_THRESHOLD;   // true on the first selected key
       const bool need_o = need && (m_ref != -INFINITY);   // O and l hold earlier blocks' mass
       const float alpha = need_o ? ex2(m_ref - mb) : 1.0f;
       if (need_o) l *= alpha;
       if (need) m_ref = mb;
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;   // no key yet: every p is 0
-      uint32_t pk[32];
+      // p = 2^x with x = s * scale * log2 e - m <= 8 rounded to fp16 and exponentiated two at a
+      // time in fp16 (P is consumed as fp16 by the PV UMMA); l sums the same fp16 values in fp32,
+      // so out = O / l divides by exactly the weights O was built from.
+      uint32_t pk[PCOLS / 2];
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2(fmaf(s[2 * c], sl2, neg_m));
-        const float p1 = ex2(fmaf(s[2 * c + 1], sl2, neg_m));
-        pk[c] = pack_f16x2(p0, p1);
-        ls[c & 3] += p0 + p1;
+      for (int c = 0; c < PCOLS / 2; ++c) {
+        pk[c] = ex2_f16x2(pack_f16x2(fmaf(s[2 * c], sl2, neg_m), fmaf(s[2 * c + 1], sl2, neg_m)));
+        ls[c & 3] = add_f16x2_to_f32(pk[c], ls[c & 3]);
       }
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       if (i > 0) {
         // P's TMEM columns and O are free once PV(i-1) has completed. A failed wait here is
-        // carried into the next block's pair barrier (or the epilogue's), so both warps of the
-        // pair leave together; the writes below then only touch this CTA's own TMEM.
+        // carried into the next block's quadrant barrier (or the epilogue's), so the quadrant's
+        // warps leave together; the writes below then only touch this CTA's own TMEM.
         const bool pv_ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_p));
         ok = ok && pv_ok;
         tc_fence_after();
         if (pv_ok && __any_sync(0xffffffffu, need_o)) {
-#pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
-            uint32_t v[32];
-            const uint32_t addr = tmem + lane_off + TM_O + static_cast<uint32_t>(half * 64 + c * 32);
-            tmem_ld_32x32b_x32(addr, v);
-            tmem_ld_wait();
+          uint32_t v[PCOLS];
+          const uint32_t addr = tmem + lane_off + TM_O + static_cast<uint32_t>(part * PCOLS);
+          tmem_ld_32x32b_x32(addr, v);
+          tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-            tmem_st_32x32b_x32(addr, v);
-          }
+          for (int e = 0; e < PCOLS; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+          tmem_st_32x32b_x32(addr, v);
         }
       }
-      tmem_st_32x32b_x32(tmem + lane_off + TM_P + half * 32, pk);
+      tmem_st_32x32b_x16(tmem + lane_off + TM_P + part * (PCOLS / 2), pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full);
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(nblk - 1) & 1], ((nblk - 1) >> 1) & 1, abort_p));
-    // partial sums go to the parity the last block did not use (its reads finished before the
-    // last block's pair barrier)
-    red_max[nblk & 1][half][r] = l;
-    ok = pair_sync_and(pair_bar, ok);
+    // Partial sums are combined through the first K stage: once the last PV has completed,
+    // every UMMA of the tile is done and no copy is in flight, so the K ring is free.
+    float* lpart = reinterpret_cast<float*>(sK);   // [NPART][BQ]
+    if (ok) lpart[part * BQ + r] = l;
+    ok = quad_sync_and(quad_bar, ok);
     if (ok) {
       tc_fence_after();
-      const float lt = l + red_max[nblk & 1][half ^ 1][r];
-      const float inv_l = (lt > 0.f) ? 1.0f / lt : 0.f;
-      uint16_t* orow = p.out + ((static_cast<int64_t>(b) * p.T + (row_valid ? t : 0)) * p.H + h) * 128 + half * 64;
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + TM_O + static_cast<uint32_t>(half * 64 + c * 32), v);
-        tmem_ld_wait();
-        if (row_valid) {
-          uint4* d4 = reinterpret_cast<uint4*>(orow + c * 32);
+      float lt = 0.f;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            d4[k] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l),
-                               pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l),
-                               pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l),
-                               pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l));
-          }
+      for (int k = 0; k < NPART; ++k) lt += lpart[k * BQ + r];   // fixed order: same sum in every part
+      const float inv_l = (lt > 0.f) ? 1.0f / lt : 0.f;
+      uint32_t v[PCOLS];
+      tmem_ld_32x32b_x32(tmem + lane_off + TM_O + static_cast<uint32_t>(part * PCOLS), v);
+      tmem_ld_wait();
+      if (row_valid) {
+        uint4* d4 = reinterpret_cast<uint4*>(
+            p.out + ((static_cast<int64_t>(b) * p.T + t) * p.H + h) * 128 + part * PCOLS);
+#pragma unroll
+        for (int k = 0; k < PCOLS / 8; ++k) {
+          d4[k] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l),
+                             pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l),
+                             pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l),
+                             pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l));
         }
-      }
-      if (row_valid && half == 0) {
-        const float lse = (lt > 0.f) ? (m_ref + log2f(lt)) * 0.6931471805599453f : -INFINITY;
-        p.lse[(static_cast<int64_t>(b) * p.T + t) * p.H + h] = lse;
+        if (part == 0) {
+          const float lse = (lt > 0.f) ? (m_ref + log2f(lt)) * 0.6931471805599453f : -INFINITY;
+          p.lse[(static_cast<int64_t>(b) * p.T + t) * p.H + h] = lse;
+        }
       }
     }
   }
