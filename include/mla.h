@@ -69,8 +69,9 @@ typedef struct {
 
 /* Bytes of device workspace mla_sparse_prefill needs for `d` (0 if `d` is invalid): the
  * up-projected keys/values kv [B, H, T, 256] fp16, the key residuals klo [B, H, T, 128] (1 byte
- * each) and the canonical selection bitsets [B, T, ceil(T/128)*4] uint32, each 1024-byte aligned
- * (see mla_kvnorm_wkvb and mla_canon_select for their contents). */
+ * each), the canonical selection bitsets [B, T, ceil(T/128)*4] uint32 (see mla_kvnorm_wkvb and
+ * mla_canon_select for their contents) and 1024 bytes holding the attention stage's tile counter,
+ * each 1024-byte aligned. Calls that run at the same time need workspaces of their own. */
 MLA_API size_t mla_sparse_prefill_workspace_size(mla_dims d);
 
 /* The whole prefill path: kv_norm -> wkv_b -> sparse causal attention.
@@ -117,7 +118,9 @@ MLA_API mla_status mla_canon_select(const int32_t* topk_idx, mla_dims d, uint32_
 MLA_API mla_status mla_kvnorm_wkvb(const mla_bf16* c_kv, const float* gamma, const mla_bf16* wkv_b, mla_dims d,
                            uint16_t* kv, uint8_t* klo, void* stream);
 
-/* Stage 4 alone: sparse causal attention from the outputs of the two stages above. */
+/* Stage 4 alone: sparse causal attention from the outputs of the two stages above. Its tile
+ * counter is one library-owned word per device, zeroed on `stream` before the launch: calls of
+ * this entry point that can overlap on one device (other streams, other threads) race on it. */
 MLA_API mla_status mla_sparse_attention(const mla_bf16* q, const mla_bf16* k_pe, const uint16_t* kv,
                                 const uint8_t* klo, const uint32_t* sel_bits, mla_bf16* out, float* lse,
                                 mla_dims d, void* stream);

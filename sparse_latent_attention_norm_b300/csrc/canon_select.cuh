@@ -18,10 +18,14 @@ namespace mla {
 constexpr int kCanonThreads = 256;
 constexpr unsigned kErrIndex = 4;
 
+// `sched` (nullable): the attention stage's tile counter, set to zero here so that the attention
+// launch that follows on the same stream starts handing out tiles from the first.
 __global__ void __launch_bounds__(kCanonThreads) canon_select_kernel(const int32_t* __restrict__ topk_idx, int T,
                                                                      int K, int W, uint32_t* __restrict__ sel_bits,
-                                                                     int32_t* __restrict__ n_keys, int validate) {
+                                                                     int32_t* __restrict__ n_keys, int validate,
+                                                                     uint32_t* __restrict__ sched) {
   extern __shared__ uint32_t bits[];
+  if (sched != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *sched = 0u;
   __shared__ int warp_counts[kCanonThreads / 32];
   const int64_t row = blockIdx.x;
   const int t = static_cast<int>(row % T);

@@ -68,16 +68,17 @@ mla_status check_dims(mla_dims d) {
 size_t kv_bytes(mla_dims d) { return static_cast<size_t>(d.B) * d.H * d.T * kKV * 2; }
 size_t klo_bytes(mla_dims d) { return static_cast<size_t>(d.B) * d.H * d.T * 128; }
 size_t bits_bytes(mla_dims d) { return static_cast<size_t>(d.B) * d.T * bits_words(d.T) * 4; }
+constexpr size_t kSchedBytes = 1024;   // the attention stage's tile counter (one word, padded)
 
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 mla_status launch_canon(const int32_t* topk_idx, mla_dims d, uint32_t* sel_bits, int32_t* n_keys, unsigned flags,
-                        cudaStream_t st) {
+                        uint32_t* sched, cudaStream_t st) {
   const int W = bits_words(d.T);
   const size_t smem = static_cast<size_t>(W) * 4;
   const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(d.B) * d.T);
   mla::canon_select_kernel<<<grid, mla::kCanonThreads, smem, st>>>(topk_idx, d.T, d.K, W, sel_bits, n_keys,
-                                                                   (flags & MLA_FLAG_VALIDATE_INDICES) ? 1 : 0);
+                                                                   (flags & MLA_FLAG_VALIDATE_INDICES) ? 1 : 0, sched);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -110,8 +111,10 @@ mla_status launch_kvnorm_wkvb(const mla_bf16* c_kv, const float* gamma, const ml
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+// `sched` must hold zero when the launch starts (the selection stage or a memset before it sets it).
 mla_status launch_sparse_attn(const mla_bf16* q, const mla_bf16* k_pe, const uint16_t* kv, const uint8_t* klo,
-                              const uint32_t* sel_bits, mla_bf16* out, float* lse, mla_dims d, cudaStream_t st) {
+                              const uint32_t* sel_bits, mla_bf16* out, float* lse, mla_dims d, uint32_t* sched,
+                              int num_sms, cudaStream_t st) {
   CUtensorMap tm_q, tm_kv, tm_kpe, tm_klo;
   {
     const uint64_t dims[4] = {kQK, static_cast<uint64_t>(d.H), static_cast<uint64_t>(d.T), static_cast<uint64_t>(d.B)};
@@ -143,15 +146,39 @@ mla_status launch_sparse_attn(const mla_bf16* q, const mla_bf16* k_pe, const uin
   p.T = d.T;
   p.H = d.H;
   p.nqt = (d.T + mla::k2::BQ - 1) / mla::k2::BQ;
+  const int64_t n_items = static_cast<int64_t>(d.B) * d.H * p.nqt;
+  if (n_items > INT32_MAX / 2) return MLA_ERR_UNSUPPORTED;
+  p.n_items = static_cast<int>(n_items);
+  p.sched = sched;
   p.W = bits_words(d.T);
   p.scale_log2 = static_cast<float>(mla_softmax_scale() * 1.4426950408889634);
   p.q = q;
   p.sel_bits = sel_bits;
   p.out = out;
   p.lse = lse;
-  const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(d.B) * d.H * p.nqt);
+  // persistent: one CTA per SM (the tiles fill its shared memory), tiles handed out dynamically
+  const unsigned grid = static_cast<unsigned>(n_items < num_sms ? n_items : num_sms);
   mla::k2::sparse_attn_kernel<<<grid, mla::k2::THREADS, mla::k2::SMEM_BYTES, st>>>(tm_q, tm_kv, tm_kpe, tm_klo, p);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+// Tile counter of the staged attention entry point, which has no workspace: one word per device,
+// zeroed on the caller's stream before each launch.
+static __device__ uint32_t g_staged_sched;
+void* g_staged_sched_ptr[kMaxDevices] = {};
+std::mutex g_staged_sched_mutex;
+
+mla_status staged_sched_counter(uint32_t** ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_staged_sched_mutex);
+  if (g_staged_sched_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_staged_sched) != cudaSuccess || p == nullptr) return MLA_ERR_CUDA;
+    g_staged_sched_ptr[dev] = p;
+  }
+  *ptr = static_cast<uint32_t*>(g_staged_sched_ptr[dev]);
+  return MLA_OK;
 }
 
 }  // namespace
@@ -180,7 +207,7 @@ const char* mla_status_string(mla_status s) {
 
 size_t mla_sparse_prefill_workspace_size(mla_dims d) {
   if (check_dims(d) != MLA_OK) return 0;
-  return align_up(kv_bytes(d), 1024) + align_up(klo_bytes(d), 1024) + align_up(bits_bytes(d), 1024);
+  return align_up(kv_bytes(d), 1024) + align_up(klo_bytes(d), 1024) + align_up(bits_bytes(d), 1024) + kSchedBytes;
 }
 
 mla_status mla_canon_select(const int32_t* topk_idx, mla_dims d, uint32_t* sel_bits, int32_t* n_keys,
@@ -191,7 +218,7 @@ mla_status mla_canon_select(const int32_t* topk_idx, mla_dims d, uint32_t* sel_b
   if (n_keys && (reinterpret_cast<uintptr_t>(n_keys) & 3u)) return MLA_ERR_INVALID_ARG;
   int sms;
   if ((s = device_setup(&sms)) != MLA_OK) return s;
-  return launch_canon(topk_idx, d, sel_bits, n_keys, flags, as_stream(stream));
+  return launch_canon(topk_idx, d, sel_bits, n_keys, flags, nullptr, as_stream(stream));
 }
 
 mla_status mla_kvnorm_wkvb(const mla_bf16* c_kv, const float* gamma, const mla_bf16* wkv_b, mla_dims d,
@@ -216,7 +243,10 @@ mla_status mla_sparse_attention(const mla_bf16* q, const mla_bf16* k_pe, const u
     return MLA_ERR_INVALID_ARG;
   int sms;
   if ((s = device_setup(&sms)) != MLA_OK) return s;
-  return launch_sparse_attn(q, k_pe, kv, klo, sel_bits, out, lse, d, as_stream(stream));
+  uint32_t* sched = nullptr;
+  if ((s = staged_sched_counter(&sched)) != MLA_OK) return s;
+  if (cudaMemsetAsync(sched, 0, sizeof(uint32_t), as_stream(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+  return launch_sparse_attn(q, k_pe, kv, klo, sel_bits, out, lse, d, sched, sms, as_stream(stream));
 }
 
 mla_status mla_sparse_prefill_ex(const mla_bf16* q, const mla_bf16* c_kv, const mla_bf16* k_pe, const float* gamma,
@@ -248,9 +278,10 @@ mla_status mla_sparse_prefill_ex(const mla_bf16* q, const mla_bf16* c_kv, const 
   uint16_t* kv = reinterpret_cast<uint16_t*>(base);
   uint8_t* klo = base + align_up(kv_bytes(d), 1024);
   uint32_t* bits = reinterpret_cast<uint32_t*>(klo + align_up(klo_bytes(d), 1024));
-  s = launch_canon(topk_idx, d, bits, n_keys, flags, st);
+  uint32_t* sched = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(bits) + align_up(bits_bytes(d), 1024));
+  s = launch_canon(topk_idx, d, bits, n_keys, flags, sched, st);
   if (s == MLA_OK) s = launch_kvnorm_wkvb(c_kv, gamma, wkv_b, d, kv, klo, sms, st);
-  if (s == MLA_OK) s = launch_sparse_attn(q, k_pe, kv, klo, bits, out, lse, d, st);
+  if (s == MLA_OK) s = launch_sparse_attn(q, k_pe, kv, klo, bits, out, lse, d, sched, sms, st);
   if (owned && cudaFreeAsync(ws, st) != cudaSuccess && s == MLA_OK) s = MLA_ERR_CUDA;
   return s;
 }
@@ -310,16 +341,18 @@ mla_status mla_sparse_prefill_noalloc(const mla_bf16* q, const mla_bf16* c_kv, c
   if ((s = device_setup(&sms)) != MLA_OK) return s;
   void* scratch = nullptr;
   if ((s = noalloc_scratch_address(&scratch)) != MLA_OK) return s;
-  // Same carve as mla_sparse_prefill_ex. Nothing in it has to start at zero: each launch writes
-  // every word the next one reads, so the previous call's leftovers are never used.
+  // Same carve as mla_sparse_prefill_ex. The only word that has to start at zero, the attention
+  // stage's tile counter, is zeroed by the selection stage; every other word is written by the
+  // launch before the one that reads it, so the previous call's leftovers are never used.
   cudaStream_t st = as_stream(stream);
   uint8_t* base = static_cast<uint8_t*>(scratch);
   uint16_t* kv = reinterpret_cast<uint16_t*>(base);
   uint8_t* klo = base + align_up(kv_bytes(d), 1024);
   uint32_t* bits = reinterpret_cast<uint32_t*>(klo + align_up(klo_bytes(d), 1024));
-  s = launch_canon(topk_idx, d, bits, nullptr, 0u, st);
+  uint32_t* sched = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(bits) + align_up(bits_bytes(d), 1024));
+  s = launch_canon(topk_idx, d, bits, nullptr, 0u, sched, st);
   if (s == MLA_OK) s = launch_kvnorm_wkvb(c_kv, gamma, wkv_b, d, kv, klo, sms, st);
-  if (s == MLA_OK) s = launch_sparse_attn(q, k_pe, kv, klo, bits, out, lse, d, st);
+  if (s == MLA_OK) s = launch_sparse_attn(q, k_pe, kv, klo, bits, out, lse, d, sched, sms, st);
   return s;
 }
 

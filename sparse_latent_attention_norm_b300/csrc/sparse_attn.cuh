@@ -9,8 +9,8 @@
 // selection stage as one bitset per query row. The [B, T, T] -inf mask is never built: each
 // softmax thread reads its row's 128-bit slice of the bitset for the key block at hand.
 //
-// One CTA = one (batch, head, 128-query tile). Key blocks of 128 run from 0 to the tile's
-// diagonal block. Per block, the score tile S[128 x 128] (fp32, TMEM, double-buffered) is
+// Work is cut into tiles of (batch, head, 128 queries); a tile's key blocks of 128 run from 0 to
+// its diagonal block. Per block, the score tile S[128 x 128] (fp32, TMEM, double-buffered) is
 //   q_nope . k_hi   8 UMMAs kind::f16, fp16: A = q_nope from TMEM, B = k_hi from shared memory
 // + q_pe . k_pe     4 UMMAs kind::f16, bf16: both from shared memory (the inputs as given)
 // + q8 . k_lo       4 UMMAs kind::f8f6f4: A = e5m2(q_nope * 2^-11), B = e4m3 residual * 2^11
@@ -27,9 +27,16 @@
 // blocks i+1 and i+2 are computed while the softmax of block i runs and PV(i) is queued as soon
 // as its probabilities are in TMEM.
 //
-// Warp roles (608 threads): warp 0 TMA producer, warp 1 TMEM owner + QK^T MMA issuer, warp 18 PV
-// MMA issuer, warps 2-17 query preparation, softmax and epilogue (warp w owns TMEM lanes
-// 32*(w%4) .. +31, i.e. 32 rows, and key / value columns 32*((w-2)/4) .. +31).
+// The kernel is persistent: one CTA per SM takes tiles from a global counter (head by head,
+// longest tile of a head first) until none are left. All roles walk the CTA's tile sequence with
+// continuous barrier phases, so the next tile's q_pe / K / V loads and its first QK^T blocks run
+// while the current tile finishes; the next tile's queries are prepared before the current
+// tile's epilogue, and its PV waits only for the epilogue to have read O.
+//
+// Warp roles (640 threads): warp 0 tile scheduler + TMA producer of q_pe and K blocks, warp 19
+// TMA producer of V blocks, warp 1 TMEM owner + QK^T MMA issuer, warp 18 PV MMA issuer, warps
+// 2-17 query preparation, softmax and epilogue (warp w owns TMEM lanes 32*(w%4) .. +31, i.e. 32
+// rows, and key / value columns 32*((w-2)/4) .. +31).
 #pragma once
 
 #include "ptx.cuh"
@@ -49,8 +56,10 @@ constexpr int NV_STAGE = 2;
 constexpr int NPART = 4;                // softmax warps per TMEM lane quadrant (column parts)
 constexpr int PCOLS = BK / NPART;       // key / value columns per softmax thread
 constexpr int NSOFT = 128 * NPART;      // softmax / epilogue threads
-constexpr int PV_WARP = 2 + NSOFT / 32; // warp 0 TMA, warp 1 QK MMA, warps 2.. softmax, then PV MMA
-constexpr int THREADS = 32 * (PV_WARP + 1);
+constexpr int PV_WARP = 2 + NSOFT / 32; // warp 0 TMA (q_pe, K), warp 1 QK MMA, warps 2.. softmax, then PV MMA,
+constexpr int VP_WARP = PV_WARP + 1;    // then TMA (V)
+constexpr int THREADS = 32 * (VP_WARP + 1);
+constexpr int NCONSUMER = 3 + NSOFT;    // threads that read each published tile index
 constexpr int TILE_BYTES = QPE_BYTES + Q8_BYTES + NK_STAGE * K_BYTES + NV_STAGE * V_BYTES;
 
 // Barriers and small shared state, placed after the tiles in the dynamic shared memory (the
@@ -59,7 +68,9 @@ constexpr int TILE_BYTES = QPE_BYTES + Q8_BYTES + NK_STAGE * K_BYTES + NV_STAGE 
 struct Ctrl {
   int max_key[3][BQ];        // [block % 3][row]: block max of the row's selected raw scores, as an
                              // order-preserving integer key, reduced with shared atomicMax
-  uint64_t q_full, q_ready, drain, drain_pv;
+  int item_idx[2];           // tile indices published by the K producer (-1: no more tiles)
+  uint64_t item_full[2], item_empty[2];
+  uint64_t q_full, q_ready, q_free, o_free, drain, drain_pv;
   uint64_t k_full[NK_STAGE], k_empty[NK_STAGE];
   uint64_t v_full[NV_STAGE], v_empty[NV_STAGE];
   uint64_t s_full[2], s_free[2], p_full, pv_done[2];
@@ -79,6 +90,8 @@ constexpr float Q8_SCALE = 1.0f / 2048.0f; // 2^-11, undoes the 2^11 on k_lo
 struct Params {
   int B, T, H;
   int nqt;                 // ceil(T / 128)
+  int n_items;             // B * H * nqt tiles
+  uint32_t* sched;         // tile counter, zero at launch; tiles are taken with atomicAdd
   int W;                   // bitset words per query row
   float scale_log2;        // softmax_scale * log2(e)
   const uint16_t* q;       // [B, T, H, 192] bf16
@@ -136,6 +149,32 @@ __device__ __forceinline__ float float_from_order_key(int k) {
   return __int_as_float(k >= 0 ? k : (k ^ 0x7FFFFFFF));
 }
 
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r) : "memory");
+}
+__device__ __forceinline__ void tmem_ld_32x32b_x4(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
+
+// Tile index -> (batch, head, query tile). Tiles run head by head (so the CTAs at work at any
+// time share a few heads' keys and values in L2) and, within a head, from the longest query tile
+// (the most key blocks) down, so the dynamic hand-out ends with short tiles.
+struct Tile {
+  int b, h, qt, t0, nblk;
+};
+__device__ __forceinline__ Tile tile_of(int item, const Params& p) {
+  Tile x;
+  const int bh = item / p.nqt;
+  x.qt = p.nqt - 1 - (item % p.nqt);
+  x.b = bh / p.H;
+  x.h = bh % p.H;
+  x.t0 = x.qt * BQ;
+  x.nblk = x.qt + 1;
+  return x;
+}
+
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -166,8 +205,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sV = sK + NK_STAGE * K_BYTES;
 
   Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem + TILE_BYTES);
+  uint64_t* item_full = ctl.item_full;
+  uint64_t* item_empty = ctl.item_empty;
   uint64_t& q_full = ctl.q_full;
   uint64_t& q_ready = ctl.q_ready;
+  uint64_t& q_free = ctl.q_free;
+  uint64_t& o_free = ctl.o_free;
   uint64_t& drain = ctl.drain;
   uint64_t& drain_pv = ctl.drain_pv;
   uint64_t* k_full = ctl.k_full;
@@ -186,19 +229,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = warp_id();
   const int lane = lane_id();
 
-  // work item: heads in order, query tiles of a head from the longest (diagonal-most) down
-  const int item = blockIdx.x;
-  const int bh = item / p.nqt;
-  const int qt = p.nqt - 1 - (item % p.nqt);
-  const int b = bh / p.H, h = bh % p.H;
-  const int t0 = qt * BQ;
-  const int nblk = qt + 1;
-
   for (int i = threadIdx.x; i < 3 * BQ; i += THREADS) (&max_key[0][0])[i] = INT_MIN;
   if (threadIdx.x == 0) {
     abort_flag = 0;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&item_full[s], 1);
+      mbar_init(&item_empty[s], NCONSUMER);
+    }
     mbar_init(&q_full, 1);
     mbar_init(&q_ready, NSOFT);
+    mbar_init(&q_free, 1);
+    mbar_init(&o_free, NSOFT);
     mbar_init(&drain, 1);
     mbar_init(&drain_pv, 1);
     for (int s = 0; s < NK_STAGE; ++s) {
@@ -232,59 +273,103 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base;
 
+  // Every role walks the same tile sequence: tile number `it` of this CTA is published in slot
+  // it & 1 of item_idx by the K producer. take_item returns the tile index (or -1 past the end)
+  // and releases the slot; false if the wait gave up.
+  auto take_item = [&](int it, int& item) -> bool {
+    const int slot = it & 1;
+    if (!mbar_wait(&item_full[slot], (it >> 1) & 1, abort_p)) return false;
+    item = ctl.item_idx[slot];
+    mbar_arrive(&item_empty[slot]);
+    return true;
+  };
+
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ scheduler + TMA producer: q_pe, K
+    // Takes the CTA's tiles from the global counter one tile ahead (the atomic's latency overlaps
+    // the current tile's loads) and publishes them to the other roles.
     if (lane == 0) {
-      const int kv_plane = b * p.H + h;
       bool ok = true;
-      bool kpend[NK_STAGE] = {}, vpend[NV_STAGE] = {};
-      uint32_t kpar[NK_STAGE] = {}, vpar[NV_STAGE] = {};
-      mbar_arrive_expect_tx(&q_full, QPE_BYTES);
-      tma_load_4d(sQpe, &tm_q, &q_full, 128, h, t0, b);
-      int ks = 0, vs = 0;
-      uint32_t kph = 0, vph = 0;
-      // K runs one block ahead of V: K(i+1) never queues behind the wait for a free V stage
-      auto load_k = [&](int i) -> bool {
-        if (!mbar_wait(&k_empty[ks], kph ^ 1, abort_p)) return false;
-        kpend[ks] = false;
-        uint8_t* kdst = sK + ks * K_BYTES;
-        const int j0 = i * BK;
-        mbar_arrive_expect_tx(&k_full[ks], K_BYTES);
-        tma_load_3d(kdst, &tm_kv, &k_full[ks], 0, j0, kv_plane);
-        tma_load_3d(kdst + ATOM_BYTES, &tm_kv, &k_full[ks], 64, j0, kv_plane);
-        tma_load_3d(kdst + 2 * ATOM_BYTES, &tm_kpe, &k_full[ks], 0, j0, b);
-        tma_load_3d(kdst + 3 * ATOM_BYTES, &tm_klo, &k_full[ks], 0, j0, kv_plane);
-        kpend[ks] = true;
-        kpar[ks] = kph;
-        if (++ks == NK_STAGE) { ks = 0; kph ^= 1; }
-        return true;
-      };
-      ok = load_k(0);
-      for (int i = 0; i < nblk && ok; ++i) {
-        if (i + 1 < nblk && !load_k(i + 1)) { ok = false; break; }
-        const int j0 = i * BK;
-        if (!mbar_wait(&v_empty[vs], vph ^ 1, abort_p)) { ok = false; break; }
-        vpend[vs] = false;
-        uint8_t* vdst = sV + vs * V_BYTES;
-        mbar_arrive_expect_tx(&v_full[vs], V_BYTES);
-        tma_load_3d(vdst, &tm_kv, &v_full[vs], 128, j0, kv_plane);
-        tma_load_3d(vdst + ATOM_BYTES, &tm_kv, &v_full[vs], 192, j0, kv_plane);
-        vpend[vs] = true;
-        vpar[vs] = vph;
-        if (++vs == NV_STAGE) { vs = 0; vph ^= 1; }
+      bool kpend[NK_STAGE] = {};
+      uint32_t kpar[NK_STAGE] = {};
+      bool qpend = false;
+      uint32_t qpar = 0;
+      int ks = 0;
+      uint32_t kph = 0;
+      int next = static_cast<int>(atomicAdd(p.sched, 1u));
+      for (int it = 0; ok; ++it) {
+        const int item = next < p.n_items ? next : -1;
+        const int slot = it & 1;
+        if (it >= 2 && !mbar_wait(&item_empty[slot], ((it - 2) >> 1) & 1, abort_p)) { ok = false; break; }
+        ctl.item_idx[slot] = item;
+        mbar_arrive(&item_full[slot]);
+        if (item < 0) break;
+        next = static_cast<int>(atomicAdd(p.sched, 1u));
+        const Tile tl = tile_of(item, p);
+        const int kv_plane = tl.b * p.H + tl.h;
+        // q_pe of this tile replaces the previous tile's once its last QK^T has completed
+        if (it >= 1 && !mbar_wait(&q_free, (it - 1) & 1, abort_p)) { ok = false; break; }
+        qpend = false;
+        mbar_arrive_expect_tx(&q_full, QPE_BYTES);
+        tma_load_4d(sQpe, &tm_q, &q_full, 128, tl.h, tl.t0, tl.b);
+        qpend = true;
+        qpar = it & 1;
+        for (int i = 0; i < tl.nblk; ++i) {
+          if (!mbar_wait(&k_empty[ks], kph ^ 1, abort_p)) { ok = false; break; }
+          uint8_t* kdst = sK + ks * K_BYTES;
+          const int j0 = i * BK;
+          mbar_arrive_expect_tx(&k_full[ks], K_BYTES);
+          tma_load_3d(kdst, &tm_kv, &k_full[ks], 0, j0, kv_plane);
+          tma_load_3d(kdst + ATOM_BYTES, &tm_kv, &k_full[ks], 64, j0, kv_plane);
+          tma_load_3d(kdst + 2 * ATOM_BYTES, &tm_kpe, &k_full[ks], 0, j0, tl.b);
+          tma_load_3d(kdst + 3 * ATOM_BYTES, &tm_klo, &k_full[ks], 0, j0, kv_plane);
+          kpend[ks] = true;
+          kpar[ks] = kph;
+          if (++ks == NK_STAGE) { ks = 0; kph ^= 1; }
+        }
       }
       if (!ok) {
         // unwinding: let the copies already issued land before shared memory goes away
-        mbar_wait(&q_full, 0, nullptr);
+        if (qpend) mbar_wait(&q_full, qpar, nullptr);
         for (int s = 0; s < NK_STAGE; ++s)
           if (kpend[s]) mbar_wait(&k_full[s], kpar[s], nullptr);
+      }
+    }
+  } else if (warp == VP_WARP) {
+    // ------------------------------------------------------------ TMA producer: V
+    // A thread of its own, so a K load never waits for a V stage to drain (and the reverse).
+    if (lane == 0) {
+      bool ok = true;
+      bool vpend[NV_STAGE] = {};
+      uint32_t vpar[NV_STAGE] = {};
+      int vs = 0;
+      uint32_t vph = 0;
+      for (int it = 0; ok; ++it) {
+        int item;
+        if (!take_item(it, item)) { ok = false; break; }
+        if (item < 0) break;
+        const Tile tl = tile_of(item, p);
+        const int kv_plane = tl.b * p.H + tl.h;
+        for (int i = 0; i < tl.nblk; ++i) {
+          if (!mbar_wait(&v_empty[vs], vph ^ 1, abort_p)) { ok = false; break; }
+          uint8_t* vdst = sV + vs * V_BYTES;
+          const int j0 = i * BK;
+          mbar_arrive_expect_tx(&v_full[vs], V_BYTES);
+          tma_load_3d(vdst, &tm_kv, &v_full[vs], 128, j0, kv_plane);
+          tma_load_3d(vdst + ATOM_BYTES, &tm_kv, &v_full[vs], 192, j0, kv_plane);
+          vpend[vs] = true;
+          vpar[vs] = vph;
+          if (++vs == NV_STAGE) { vs = 0; vph ^= 1; }
+        }
+      }
+      if (!ok) {
         for (int s = 0; s < NV_STAGE; ++s)
           if (vpend[s]) mbar_wait(&v_full[s], vpar[s], nullptr);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ QK^T MMA issuer
-    // Scores of block i go to S buffer i & 1 once the softmax has read block i-2 out of it.
+    // Scores of global block g go to S buffer g & 1 once the softmax has read block g-2 out of it.
     if (lane == 0) {
       const uint32_t idesc_nope = idesc_f32acc(BQ, BK, kFmtF16, false, false);
       const uint32_t idesc_rope = idesc_f32acc(BQ, BK, kFmtBF16, false, false);
@@ -298,30 +383,40 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint64_t d_qpe = sdesc_sw128(smem_u32(sQpe), 16, 1024);
       const uint64_t d_q8 = sdesc_sw128(smem_u32(sQ8), 16, 1024);
       bool issued = false;
+      bool ok = true;
       int ks = 0;
       uint32_t kph = 0;
-      bool ok = mbar_wait(&q_full, 0, abort_p) && mbar_wait(&q_ready, 0, abort_p);
-      for (int i = 0; i < nblk && ok; ++i) {
-        const int sb = i & 1;
-        if (i >= 2 && !mbar_wait(&s_free[sb], ((i - 2) >> 1) & 1, abort_p)) { ok = false; break; }
-        if (!mbar_wait(&k_full[ks], kph, abort_p)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t d = tmem + TM_S + static_cast<uint32_t>(sb * BK);
-        const uint64_t dk = ks ? d_k1 : d_k0;
+      int g = 0;   // global block counter of this CTA
+      for (int it = 0; ok; ++it) {
+        int item;
+        if (!take_item(it, item)) break;
+        if (item < 0) break;
+        const Tile tl = tile_of(item, p);
+        if (!mbar_wait(&q_full, it & 1, abort_p) || !mbar_wait(&q_ready, it & 1, abort_p)) break;
+        for (int i = 0; i < tl.nblk; ++i, ++g) {
+          const int sb = g & 1;
+          if (g >= 2 && !mbar_wait(&s_free[sb], ((g - 2) >> 1) & 1, abort_p)) { ok = false; break; }
+          if (!mbar_wait(&k_full[ks], kph, abort_p)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d = tmem + TM_S + static_cast<uint32_t>(sb * BK);
+          const uint64_t dk = ks ? d_k1 : d_k0;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)   // q_nope (TMEM, fp16) . k_hi
-          umma_ts(d, tmem + TM_QN + kk * 8, dk + (((kk >> 2) * ATOM_BYTES + (kk & 3) * 32) >> 4), idesc_nope,
-                  kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk)   // q_nope (TMEM, fp16) . k_hi
+            umma_ts(d, tmem + TM_QN + kk * 8, dk + (((kk >> 2) * ATOM_BYTES + (kk & 3) * 32) >> 4), idesc_nope,
+                    kk > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)   // q_pe . k_pe (bf16)
-          umma_ss(d, d_qpe + kk * 2, dk + ((2 * ATOM_BYTES + kk * 32) >> 4), idesc_rope, 1u);
+          for (int kk = 0; kk < 4; ++kk)   // q_pe . k_pe (bf16)
+            umma_ss(d, d_qpe + kk * 2, dk + ((2 * ATOM_BYTES + kk * 32) >> 4), idesc_rope, 1u);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)   // e5m2(q_nope 2^-11) . e4m3(k_lo 2^11)
-          umma_f8_ss(d, d_q8 + kk * 2, dk + ((3 * ATOM_BYTES + kk * 32) >> 4), idesc_lo, 1u);
-        issued = true;
-        umma_commit(&k_empty[ks]);
-        umma_commit(&s_full[sb]);
-        if (++ks == NK_STAGE) { ks = 0; kph ^= 1; }
+          for (int kk = 0; kk < 4; ++kk)   // e5m2(q_nope 2^-11) . e4m3(k_lo 2^11)
+            umma_f8_ss(d, d_q8 + kk * 2, dk + ((3 * ATOM_BYTES + kk * 32) >> 4), idesc_lo, 1u);
+          issued = true;
+          umma_commit(&k_empty[ks]);
+          umma_commit(&s_full[sb]);
+          if (++ks == NK_STAGE) { ks = 0; kph ^= 1; }
+        }
+        // the tile's q_pe, q8 and q_nope are free once its last QK^T has completed
+        if (ok) umma_commit(&q_free);
       }
       if (issued) {
         // every MMA this thread issued has finished before TMEM is released
@@ -339,21 +434,31 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint64_t d_v0 = sdesc_sw128(smem_u32(sV), ATOM_BYTES, 1024);
       const uint64_t d_v1 = sdesc_sw128(smem_u32(sV + V_BYTES), ATOM_BYTES, 1024);
       bool issued = false;
+      bool ok = true;
       int vs = 0;
       uint32_t vph = 0;
-      for (int i = 0; i < nblk; ++i) {
-        // PV(i): P(i) from TMEM, V(i) from shared memory
-        if (!mbar_wait(&p_full, i & 1, abort_p)) break;
-        if (!mbar_wait(&v_full[vs], vph, abort_p)) break;
-        tc_fence_after();
-        const uint64_t dv = vs ? d_v1 : d_v0;
+      int g = 0;
+      for (int it = 0; ok; ++it) {
+        int item;
+        if (!take_item(it, item)) break;
+        if (item < 0) break;
+        const Tile tl = tile_of(item, p);
+        // O is rewritten from the tile's first block on: the previous tile's epilogue must have read it
+        if (it >= 1 && !mbar_wait(&o_free, (it - 1) & 1, abort_p)) break;
+        for (int i = 0; i < tl.nblk; ++i, ++g) {
+          // PV(g): P(g) from TMEM, V(g) from shared memory
+          if (!mbar_wait(&p_full, g & 1, abort_p)) { ok = false; break; }
+          if (!mbar_wait(&v_full[vs], vph, abort_p)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t dv = vs ? d_v1 : d_v0;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)   // 16 keys per UMMA: 16 rows of 128 bytes = 2048 bytes
-          umma_ts(tmem + TM_O, tmem + TM_P + kk * 8, dv + ((kk * 2048) >> 4), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-        issued = true;
-        umma_commit(&v_empty[vs]);
-        umma_commit(&pv_done[i & 1]);   // PV(i) is completion i >> 1 of pv_done[i & 1]
-        if (++vs == NV_STAGE) { vs = 0; vph ^= 1; }
+          for (int kk = 0; kk < 8; ++kk)   // 16 keys per UMMA: 16 rows of 128 bytes = 2048 bytes
+            umma_ts(tmem + TM_O, tmem + TM_P + kk * 8, dv + ((kk * 2048) >> 4), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+          issued = true;
+          umma_commit(&v_empty[vs]);
+          umma_commit(&pv_done[g & 1]);   // PV(g) is completion g >> 1 of pv_done[g & 1]
+          if (++vs == NV_STAGE) { vs = 0; vph ^= 1; }
+        }
       }
       if (issued) {
         umma_commit(&drain_pv);
@@ -371,16 +476,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int qw = warp & 3;
     const int part = (warp - 2) >> 2;
     const int r = qw * 32 + lane;           // query row in the tile == TMEM lane
-    const int t = t0 + r;
-    const bool row_valid = t < p.T;
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
     const int quad_bar = 1 + qw;
+    const float sl2 = p.scale_log2;
 
-    // q_nope[32*part .. +31] of row r: fp16 pairs into TMEM (exact for bf16 values within fp16's
-    // range), and e5m2(q_nope * 2^-11) into the swizzled q8 tile (16-byte chunk c at c ^ (r & 7)).
-    {
+    // q_nope[32*part .. +31] of row r of tile `tl`: fp16 pairs into TMEM (exact for bf16 values
+    // within fp16's range), and e5m2(q_nope * 2^-11) into the swizzled q8 tile (16-byte chunk c at
+    // c ^ (r & 7)). Called once the previous tile's QK^T UMMAs have all completed.
+    auto prepare_queries = [&](const Tile& tl) {
+      const int t = tl.t0 + r;
+      const bool row_valid = t < p.T;
       const uint4* qrow = reinterpret_cast<const uint4*>(
-          p.q + ((static_cast<int64_t>(b) * p.T + (row_valid ? t : 0)) * p.H + h) * 192);
+          p.q + ((static_cast<int64_t>(tl.b) * p.T + (row_valid ? t : 0)) * p.H + tl.h) * 192);
       uint32_t qn[16];
       uint32_t q8[8];
 #pragma unroll
@@ -410,114 +517,145 @@ __global__ void __launch_bounds__(THREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&q_ready);
-    }
+    };
 
-    // this thread's selection word of block i: keys PCOLS*part .. +31 of the block
-    const uint32_t* bits_row =
-        p.sel_bits + (static_cast<int64_t>(b) * p.T + (row_valid ? t : 0)) * p.W + part;
-    const float sl2 = p.scale_log2;
-    float m_ref = -INFINITY;   // running reference max, log2 domain (identical in the quadrant's warps)
-    float l = 0.f;             // running sum of this thread's columns' probabilities
     bool ok = true;
-    uint32_t mask_next = row_valid ? __ldg(bits_row) : 0u;
-    for (int i = 0; i < nblk; ++i) {
-      const uint32_t mask = mask_next;
-      if (i + 1 < nblk) mask_next = row_valid ? __ldg(bits_row + (i + 1) * 4) : 0u;
-      const int sb = i & 1;
-      const int slot = i % 3;
-      bool got = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (i >> 1) & 1, abort_p));
-      float s[PCOLS];
-      if (got) {
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, mask != 0u)) {
-          uint32_t v[PCOLS];
-          tmem_ld_32x32b_x32(tmem + lane_off + TM_S + static_cast<uint32_t>(sb * BK + part * PCOLS), v);
-          tmem_ld_wait();
+    int g = 0;        // global block counter of this CTA
+    int it = 0;
+    int item = -1;
+    {
+      const bool got = take_item(0, item);
+      ok = quad_sync_and(quad_bar, got);
+    }
+    if (ok && item >= 0) prepare_queries(tile_of(item, p));
+    while (ok && item >= 0) {
+      const Tile tl = tile_of(item, p);
+      const int t = tl.t0 + r;
+      const bool row_valid = t < p.T;
+      // this thread's selection word of block i: keys PCOLS*part .. +31 of the block
+      const uint32_t* bits_row =
+          p.sel_bits + (static_cast<int64_t>(tl.b) * p.T + (row_valid ? t : 0)) * p.W + part;
+      float m_ref = -INFINITY;   // running reference max, log2 domain (identical in the quadrant's warps)
+      float l = 0.f;             // running sum of this thread's columns' probabilities
+      uint32_t mask_next = row_valid ? __ldg(bits_row) : 0u;
+      for (int i = 0; i < tl.nblk; ++i, ++g) {
+        const uint32_t mask = mask_next;
+        if (i + 1 < tl.nblk) mask_next = row_valid ? __ldg(bits_row + (i + 1) * 4) : 0u;
+        const int sb = g & 1;
+        const int slot = g % 3;
+        bool got = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (g >> 1) & 1, abort_p));
+        float s[PCOLS];
+        if (got) {
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, mask != 0u)) {
+            uint32_t v[PCOLS];
+            tmem_ld_32x32b_x32(tmem + lane_off + TM_S + static_cast<uint32_t>(sb * BK + part * PCOLS), v);
+            tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < PCOLS; ++e) s[e] = ((mask >> e) & 1u) ? __uint_as_float(v[e]) : -INFINITY;
+            for (int e = 0; e < PCOLS; ++e) s[e] = ((mask >> e) & 1u) ? __uint_as_float(v[e]) : -INFINITY;
+          } else {
+#pragma unroll
+            for (int e = 0; e < PCOLS; ++e) s[e] = -INFINITY;
+          }
+          tc_fence_before();
+          mbar_arrive(&s_free[sb]);
         } else {
 #pragma unroll
           for (int e = 0; e < PCOLS; ++e) s[e] = -INFINITY;
         }
-        tc_fence_before();
-        mbar_arrive(&s_free[sb]);
-      } else {
+        // raw (unscaled) block max of the selected scores; the scale is positive, so scaling
+        // the max gives the max of the scaled scores exactly
+        float mx[4];   // four independent chains: mx[k] covers columns congruent to k mod 4
 #pragma unroll
-        for (int e = 0; e < PCOLS; ++e) s[e] = -INFINITY;
-      }
-      // raw (unscaled) block max of the selected scores; the scale is positive, so scaling
-      // the max gives the max of the scaled scores exactly
-      float mx[4];   // four independent chains: mx[k] covers columns congruent to k mod 4
+        for (int k = 0; k < 4; ++k) mx[k] = fmaxf(s[k], s[4 + k]);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) mx[k] = fmaxf(s[k], s[4 + k]);
+        for (int e = 8; e < PCOLS; e += 8)
 #pragma unroll
-      for (int e = 8; e < PCOLS; e += 8)
+          for (int k = 0; k < 4; ++k) mx[k] = max3f(mx[k], s[e + k], s[e + 4 + k]);
+        atomicMax(&max_key[slot][r], float_order_key(max3f(mx[0], mx[1], fmaxf(mx[2], mx[3]))));
+        ok = quad_sync_and(quad_bar, ok && got);
+        if (!ok) break;
+        const float mb = float_from_order_key(max_key[slot][r]) * sl2;
+        // the slot of block g-1 has been read by every warp of the quadrant (each read it before
+        // arriving at this block's barrier); it is next written at block g+2, after the next barrier
+        if (part == 0 && g > 0) max_key[(g + 2) % 3][r] = INT_MIN;
+        const bool need = mb > m_ref + RESCALE_THRESHOLD;   // true on the first selected key
+        const bool need_o = need && (m_ref != -INFINITY);   // O and l hold earlier blocks' mass
+        const float alpha = need_o ? ex2(m_ref - mb) : 1.0f;
+        if (need_o) l *= alpha;
+        if (need) m_ref = mb;
+        const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;   // no key yet: every p is 0
+        // p = 2^x with x = s * scale * log2 e - m <= 8 rounded to fp16 and exponentiated two at a
+        // time in fp16 (P is consumed as fp16 by the PV UMMA); l sums the same fp16 values in
+        // fp32, so out = O / l divides by exactly the weights O was built from.
+        uint32_t pk[PCOLS / 2];
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) mx[k] = max3f(mx[k], s[e + k], s[e + 4 + k]);
-      atomicMax(&max_key[slot][r], float_order_key(max3f(mx[0], mx[1], fmaxf(mx[2], mx[3]))));
-      ok = quad_sync_and(quad_bar, ok && got);
-      if (!ok) break;
-      const float mb = float_from_order_key(max_key[slot][r]) * sl2;
-      // the slot of block i-1 has been read by every warp of the quadrant (each read it before
-      // arriving at this block's barrier); it is next written at block i+2, after the next barrier
-      if (part == 0 && i > 0) max_key[(i + 2) % 3][r] = INT_MIN;
-      const bool need = mb > m_ref + RESCALE_THRESHOLD;   // true on the first selected key
-      const bool need_o = need && (m_ref != -INFINITY);   // O and l hold earlier blocks' mass
-      const float alpha = need_o ? ex2(m_ref - mb) : 1.0f;
-      if (need_o) l *= alpha;
-      if (need) m_ref = mb;
-      const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;   // no key yet: every p is 0
-      // p = 2^x with x = s * scale * log2 e - m <= 8 rounded to fp16 and exponentiated two at a
-      // time in fp16 (P is consumed as fp16 by the PV UMMA); l sums the same fp16 values in fp32,
-      // so out = O / l divides by exactly the weights O was built from.
-      uint32_t pk[PCOLS / 2];
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < PCOLS / 2; ++c) {
-        pk[c] = ex2_f16x2(pack_f16x2(fmaf(s[2 * c], sl2, neg_m), fmaf(s[2 * c + 1], sl2, neg_m)));
-        ls[c & 3] = add_f16x2_to_f32(pk[c], ls[c & 3]);
-      }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      if (i > 0) {
-        // P's TMEM columns and O are free once PV(i-1) has completed. A failed wait here is
-        // carried into the next block's quadrant barrier (or the epilogue's), so the quadrant's
-        // warps leave together; the writes below then only touch this CTA's own TMEM.
-        const bool pv_ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_p));
-        ok = ok && pv_ok;
-        tc_fence_after();
-        if (pv_ok && __any_sync(0xffffffffu, need_o)) {
-          uint32_t v[PCOLS];
-          const uint32_t addr = tmem + lane_off + TM_O + static_cast<uint32_t>(part * PCOLS);
-          tmem_ld_32x32b_x32(addr, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < PCOLS; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-          tmem_st_32x32b_x32(addr, v);
+        for (int c = 0; c < PCOLS / 2; ++c) {
+          pk[c] = ex2_f16x2(pack_f16x2(fmaf(s[2 * c], sl2, neg_m), fmaf(s[2 * c + 1], sl2, neg_m)));
+          ls[c & 3] = add_f16x2_to_f32(pk[c], ls[c & 3]);
         }
-      }
-      tmem_st_32x32b_x16(tmem + lane_off + TM_P + part * (PCOLS / 2), pk);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&p_full);
-    }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(nblk - 1) & 1], ((nblk - 1) >> 1) & 1, abort_p));
-    // Partial sums are combined through the first K stage: once the last PV has completed,
-    // every UMMA of the tile is done and no copy is in flight, so the K ring is free.
-    float* lpart = reinterpret_cast<float*>(sK);   // [NPART][BQ]
-    if (ok) lpart[part * BQ + r] = l;
-    ok = quad_sync_and(quad_bar, ok);
-    if (ok) {
-      tc_fence_after();
-      float lt = 0.f;
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        if (i > 0) {
+          // P's TMEM columns and O are free once PV(g-1) has completed (for a tile's first block
+          // the previous tile's epilogue waited for that). A failed wait here is carried into the
+          // next quadrant barrier, so the quadrant's warps leave together; the writes below then
+          // only touch this CTA's own TMEM.
+          const bool pv_ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_p));
+          ok = ok && pv_ok;
+          tc_fence_after();
+          if (pv_ok && __any_sync(0xffffffffu, need_o)) {
+            uint32_t v[PCOLS];
+            const uint32_t addr = tmem + lane_off + TM_O + static_cast<uint32_t>(part * PCOLS);
+            tmem_ld_32x32b_x32(addr, v);
+            tmem_ld_wait();
 #pragma unroll
-      for (int k = 0; k < NPART; ++k) lt += lpart[k * BQ + r];   // fixed order: same sum in every part
-      const float inv_l = (lt > 0.f) ? 1.0f / lt : 0.f;
+            for (int e = 0; e < PCOLS; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tmem_st_32x32b_x32(addr, v);
+          }
+        }
+        tmem_st_32x32b_x16(tmem + lane_off + TM_P + part * (PCOLS / 2), pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full);
+      }
+      if (!ok) break;
+
+      // The next tile's queries go in now, so its first QK^T blocks overlap this tile's epilogue:
+      // every QK^T of this tile has completed (its last scores were read above).
+      int next_item = -1;
+      {
+        const bool got = take_item(it + 1, next_item);
+        ok = quad_sync_and(quad_bar, got);
+      }
+      if (ok && next_item >= 0) prepare_queries(tile_of(next_item, p));
+
+      // epilogue: out = O / l (bf16), lse = (m + log2 l) ln 2
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_p));
+      // the row sum's four parts meet in TMEM: P's columns are idle until the next tile's first
+      // block, which every part reaches only after the barrier below
+      if (ok) {
+        tc_fence_after();
+        tmem_st_32x32b_x1(tmem + lane_off + TM_P + part, __float_as_uint(l));
+        tmem_st_wait();
+        tc_fence_before();
+      }
+      ok = quad_sync_and(quad_bar, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t lp[4];
+      tmem_ld_32x32b_x4(tmem + lane_off + TM_P, lp);
       uint32_t v[PCOLS];
       tmem_ld_32x32b_x32(tmem + lane_off + TM_O + static_cast<uint32_t>(part * PCOLS), v);
       tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&o_free);   // O is in registers: the next tile's PV may overwrite it
+      const float lt = (__uint_as_float(lp[0]) + __uint_as_float(lp[1])) +
+                       (__uint_as_float(lp[2]) + __uint_as_float(lp[3]));   // same order in every part
+      const float inv_l = (lt > 0.f) ? 1.0f / lt : 0.f;
       if (row_valid) {
         uint4* d4 = reinterpret_cast<uint4*>(
-            p.out + ((static_cast<int64_t>(b) * p.T + t) * p.H + h) * 128 + part * PCOLS);
+            p.out + ((static_cast<int64_t>(tl.b) * p.T + t) * p.H + tl.h) * 128 + part * PCOLS);
 #pragma unroll
         for (int k = 0; k < PCOLS / 8; ++k) {
           d4[k] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l),
@@ -527,9 +665,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (part == 0) {
           const float lse = (lt > 0.f) ? (m_ref + log2f(lt)) * 0.6931471805599453f : -INFINITY;
-          p.lse[(static_cast<int64_t>(b) * p.T + t) * p.H + h] = lse;
+          p.lse[(static_cast<int64_t>(tl.b) * p.T + t) * p.H + tl.h] = lse;
         }
       }
+      item = next_item;
+      ++it;
     }
   }
 

@@ -56,7 +56,8 @@ def test_workspace_size():
         klo = B * H * T * 128
         bits = B * T * ((T + 127) // 128 * 4) * 4
         up = lambda x: (x + 1023) // 1024 * 1024
-        assert mla.workspace_size(B, T, H, K) == up(kv) + up(klo) + up(bits)
+        sched = 1024   # the attention stage's tile counter
+        assert mla.workspace_size(B, T, H, K) == up(kv) + up(klo) + up(bits) + sched
     assert mla.workspace_size(0, 64, 4, 32) == 0
     assert mla.workspace_size(1, 64, 129, 32) == 0
     assert mla.workspace_size(1, 65537, 4, 32) == 0
