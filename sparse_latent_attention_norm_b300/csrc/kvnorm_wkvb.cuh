@@ -1,4 +1,5 @@
-// Stages 2-3: kv_norm fused into the wkv_b up-projection (tcgen05 GEMM, TMA-fed, TMEM accumulators).
+// Stages 2-3: kv_norm fused into the wkv_b up-projection (tcgen05 GEMM: A in TMEM, W in by TMA,
+// outputs out by TMA tensor stores).
 //
 //   y[r, :]  = bf16( gamma * (c_kv[r, :] * (1 / sqrt(mean(c_kv[r, :]^2) + 1e-6))) )
 //              (RMSNorm class, model.py 281-293: x.float(), mean of squares, x * rsqrt(var + eps),
@@ -6,7 +7,7 @@
 //              Computed in fp32 as the excerpt does, in a fixed order: squares summed in
 //              ascending feature order, IEEE-rounded sqrt and division, no fused multiply-adds.
 //   kv[r, n] = sum_c y[r, c] * wkv_b[n, c]   (ColumnParallelLinear, weight [out, in])
-// with r = b*T + t and n = h*256 + f ("Keys" page: kv.view(B, T, H, 256), split [128 | 128] into
+// with r = (b, t) and n = h*256 + f ("Keys" page: kv.view(B, T, H, 256), split [128 | 128] into
 // k_nope and v). Outputs, head-major so the attention stage reads each head's keys and values as
 // contiguous blocks:
 //   kv  [B, H, T, 256] fp16:  k_hi = fp16(k_nope) in features 0..127, fp16(v) in 128..255
@@ -14,15 +15,19 @@
 // k_hi + klo * 2^-11 carries k_nope to about 2^-14 relative, enough for lse to 1e-3 on rows
 // whose softmax sits on one or two keys; fp16 alone (2^-11) is not.
 //
-// Tiling: one unit = 128 rows x one head (256 output features) x the whole latent (512). The A
-// tile (128 x 512 bf16, 128 KB) stays in shared memory while a CTA walks the heads of its row
-// tile; it is loaded by TMA, normalised in place (the norm's only input is that row), and then
-// used by 32 UMMAs (M=128, N=256, K=16) per head. W streams through a 3-stage TMA ring of
-// 256 x 64 slices. Accumulators are double-buffered in TMEM (2 x 256 columns) so the epilogue of
-// one head overlaps the MMAs of the next.
+// Tiling: a row tile is 128 positions of one batch (the last tile of a batch may be partial); a
+// unit is one row tile x one half of one head (k_nope: W rows h*256 + [0,128), or v: h*256 +
+// [128,256)) x the whole latent (512). The normalised row tile y (128 x 512 bf16) lives in TMEM
+// (256 columns, bf16 pairs) as the A operand of every unit of the tile; W streams through a
+// 6-stage TMA ring of 128 x 64 slices (B operand), and each unit is 32 UMMAs M=128 N=128 K=16
+// into one of two TMEM accumulators, so a unit's epilogue overlaps the next unit's MMAs. The
+// epilogue converts the accumulator, writes it 128-byte-swizzled into one of two shared staging
+// buffers and TMA-stores it (kv: two 64-column boxes, klo: one box); rows past T are clipped by
+// the tensor map. A CTA takes a contiguous range of units, row-tile-major, so it normalises at
+// most a few row tiles.
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-5
-// normalise A and run the epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
+// Warp roles (192 threads): warp 0 TMA producer of W, warp 1 TMEM owner + MMA issuer, warps 2-5
+// normalise rows into TMEM and run the epilogue (warp w owns TMEM lanes 32*(w%4) .. +31).
 #pragma once
 
 #include "ptx.cuh"
@@ -30,60 +35,89 @@
 namespace mla {
 namespace k1 {
 
-constexpr int BM = 128;
-constexpr int BN = 256;                      // one head: 128 k_nope + 128 v features
-constexpr int KDIM = 512;                    // kv_lora_rank
-constexpr int KATOM = 64;                    // bf16 elements per 128-byte swizzle row
-constexpr int NKATOM = KDIM / KATOM;         // 8
-constexpr int A_ATOM_BYTES = BM * 128;       // 16 KB
-constexpr int A_BYTES = NKATOM * A_ATOM_BYTES;  // 128 KB
-constexpr int B_STAGE_BYTES = BN * 128;      // 32 KB
-constexpr int NSTAGE = 3;
+constexpr int BM = 128;                         // positions per row tile
+constexpr int BN = 128;                         // outputs per unit (k_nope or v of one head)
+constexpr int KDIM = 512;                       // kv_lora_rank
+constexpr int KATOM = 64;                       // bf16 elements per 128-byte swizzle row
+constexpr int NKATOM = KDIM / KATOM;            // 8
+constexpr int B_STAGE_BYTES = BN * 128;         // 16 KB: 128 W rows x 64 latent features
+constexpr int NSTAGE = 6;
+constexpr int OUT_ATOM = BM * 128;              // 16 KB: 128 rows x 128 bytes, 128-byte swizzle
+constexpr int OUT_STAGE_BYTES = 3 * OUT_ATOM;   // kv: two atoms (128 fp16 columns); klo: one atom
+constexpr int NOUT = 2;
 constexpr int THREADS = 192;
-constexpr int SMEM_BYTES = A_BYTES + NSTAGE * B_STAGE_BYTES + 1024;  // + alignment slack
+constexpr int TILE_BYTES = NSTAGE * B_STAGE_BYTES + NOUT * OUT_STAGE_BYTES;
+
+// Barriers after the tiles in the dynamic shared memory (no static shared memory: the dynamic
+// region then starts 1024-byte aligned, as the 128-byte swizzle needs).
+struct Ctrl {
+  uint64_t a_free, a_ready, drain;
+  uint64_t b_full[NSTAGE], b_empty[NSTAGE];
+  uint64_t acc_full[2], acc_empty[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+constexpr int SMEM_BYTES = TILE_BYTES + static_cast<int>(sizeof(Ctrl));
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_A = 0;      // y as bf16 pairs, columns 0..255 (feature f in column f / 2)
+constexpr uint32_t TM_ACC = 256;  // accumulators at columns 256..383 and 384..511
 constexpr float RMS_EPS = 1e-6f;
+constexpr float KLO_SCALE = 2048.0f;   // 2^11
+constexpr int EPI_BAR = 1;             // named barrier of the four epilogue warps
 
 struct Params {
-  int M;          // B * T rows
-  int T;          // positions per batch (row r -> b = r / T, t = r % T)
-  int H;          // heads
-  int units;      // ceil(M / 128) * H
-  const float* gamma;
-  uint16_t* kv;   // [B, H, T, 256] fp16 (k_hi | v)
-  uint8_t* klo;   // [B, H, T, 128] e4m3 ((k_nope - k_hi) * 2^11)
+  int B, T, H;
+  int mt_per_b;            // row tiles per batch: ceil(T / 128)
+  int units;               // B * mt_per_b * H * 2
+  const uint16_t* c_kv;    // [B, T, 512] bf16
+  const float* gamma;      // [512]
 };
 
-constexpr float KLO_SCALE = 2048.0f;   // 2^11
+// Named barrier of the epilogue warps that also ANDs `pred` over their 128 threads.
+__device__ __forceinline__ bool epi_sync_and(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "n"(EPI_BAR)
+      : "memory");
+  return r != 0;
+}
 
 __global__ void __launch_bounds__(THREADS, 1)
-    kvnorm_wkvb_kernel(const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_w,
-                       const Params p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + A_BYTES;
-
-  __shared__ uint64_t a_full, a_ready, a_free, drain;
-  __shared__ uint64_t b_full[NSTAGE], b_empty[NSTAGE];
-  __shared__ uint64_t acc_full[2], acc_empty[2];
-  __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag;
-  volatile int* abort_p = &abort_flag;
+    kvnorm_wkvb_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_kv,
+                       const __grid_constant__ CUtensorMap tm_klo, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) set_error(kErrUnsupportedLayout);
+    return;
+  }
+  uint8_t* sB = smem_raw;
+  uint8_t* sOut = smem_raw + NSTAGE * B_STAGE_BYTES;
+  Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem_raw + TILE_BYTES);
+  uint64_t& a_free = ctl.a_free;
+  uint64_t& a_ready = ctl.a_ready;
+  uint64_t& drain = ctl.drain;
+  uint64_t* b_full = ctl.b_full;
+  uint64_t* b_empty = ctl.b_empty;
+  uint64_t* acc_full = ctl.acc_full;
+  uint64_t* acc_empty = ctl.acc_empty;
+  volatile int* abort_p = &ctl.abort_flag;
 
   const int warp = warp_id();
   const int lane = lane_id();
 
-  // contiguous range of units for this CTA, m-major (u -> m = u / H, h = u % H)
+  // contiguous range of units for this CTA: u -> row tile m = u / (2H), head (u / 2) % H, half u % 2
   const int G = gridDim.x;
   const int u_begin = static_cast<int>((static_cast<int64_t>(p.units) * blockIdx.x) / G);
   const int u_end = static_cast<int>((static_cast<int64_t>(p.units) * (blockIdx.x + 1)) / G);
 
   if (threadIdx.x == 0) {
-    abort_flag = 0;
-    mbar_init(&a_full, 1);
-    mbar_init(&a_ready, 128);
+    ctl.abort_flag = 0;
     mbar_init(&a_free, 1);
+    mbar_init(&a_ready, 128);
     mbar_init(&drain, 1);
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&b_full[s], 1);
@@ -96,47 +130,33 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base, TMEM_COLS);
+    tmem_alloc(&ctl.tmem_base, TMEM_COLS);
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_ckv);
     tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_kv);
+    tma_prefetch_desc(&tm_klo);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = tmem_base;
+  const uint32_t tmem = ctl.tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer
+    // ------------------------------------------------ TMA producer: W slices
     if (lane == 0) {
-      int cur_m = -1, seg = 0, stage = 0;
+      int stage = 0;
       uint32_t phase = 0;
-      bool a_pending = false;
-      uint32_t a_parity = 0;
       bool pending[NSTAGE] = {};
       uint32_t pend_parity[NSTAGE] = {};
       bool ok = true;
       for (int u = u_begin; u < u_end && ok; ++u) {
-        const int m = u / p.H, h = u % p.H;
-        if (m != cur_m) {
-          if (seg > 0) {
-            if (!mbar_wait(&a_free, (seg - 1) & 1, abort_p)) { ok = false; break; }
-            a_pending = false;
-          }
-          mbar_arrive_expect_tx(&a_full, A_BYTES);
-          for (int a = 0; a < NKATOM; ++a) tma_load_2d(sA + a * A_ATOM_BYTES, &tm_ckv, &a_full, a * KATOM, m * BM);
-          a_pending = true;
-          a_parity = seg & 1;
-          cur_m = m;
-          ++seg;
-        }
+        const int h = (u >> 1) % p.H, half = u & 1;
         for (int ka = 0; ka < NKATOM; ++ka) {
           if (!mbar_wait(&b_empty[stage], phase ^ 1, abort_p)) { ok = false; break; }
-          pending[stage] = false;
           mbar_arrive_expect_tx(&b_full[stage], B_STAGE_BYTES);
-          tma_load_2d(sB + stage * B_STAGE_BYTES, &tm_w, &b_full[stage], ka * KATOM, h * BN);
+          tma_load_2d(sB + stage * B_STAGE_BYTES, &tm_w, &b_full[stage], ka * KATOM, h * 256 + half * BN);
           pending[stage] = true;
           pend_parity[stage] = phase;
           if (++stage == NSTAGE) { stage = 0; phase ^= 1; }
@@ -146,20 +166,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         // unwinding: let the copies already issued land before the CTA's shared memory goes away
         for (int s = 0; s < NSTAGE; ++s)
           if (pending[s]) mbar_wait(&b_full[s], pend_parity[s], nullptr);
-        if (a_pending) mbar_wait(&a_full, a_parity, nullptr);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(BM, BN, false, false);
-      const uint32_t sa = smem_u32(sA), sb = smem_u32(sB);
+      const uint64_t d_b0 = sdesc_sw128(smem_u32(sB), 16, 1024);   // + stage * (16 KB >> 4) + k4 * 2
       int cur_m = -1, seg = 0, stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool issued = false;
       for (int u = u_begin; u < u_end; ++u) {
-        const int m = u / p.H;
+        const int m = u / (2 * p.H);
         if (m != cur_m) {
+          // a new row tile: y in TMEM is rewritten once every MMA issued so far has completed
           if (seg > 0) umma_commit(&a_free);
           if (!mbar_wait(&a_ready, seg & 1, abort_p)) break;
           tc_fence_after();
@@ -168,17 +188,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_p)) break;
         tc_fence_after();
-        const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
+        const uint32_t d = tmem + TM_ACC + static_cast<uint32_t>(acc * BN);
         bool ok = true;
         for (int ka = 0; ka < NKATOM; ++ka) {
           if (!mbar_wait(&b_full[stage], phase, abort_p)) { ok = false; break; }
           tc_fence_after();
+          const uint64_t db = d_b0 + static_cast<uint64_t>(stage * (B_STAGE_BYTES >> 4));
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const uint64_t ad = sdesc_sw128(sa + ka * A_ATOM_BYTES + k4 * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(sb + stage * B_STAGE_BYTES + k4 * 32, 16, 1024);
-            umma_ss(d, ad, bd, idesc, (ka | k4) != 0 ? 1u : 0u);
-          }
+          for (int k4 = 0; k4 < 4; ++k4)
+            umma_ts(d, tmem + TM_A + static_cast<uint32_t>((ka * 4 + k4) * 8), db + k4 * 2, idesc,
+                    (ka | k4) != 0 ? 1u : 0u);
           issued = true;
           umma_commit(&b_empty[stage]);
           if (++stage == NSTAGE) { stage = 0; phase ^= 1; }
@@ -196,111 +215,130 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ------------------------------------------------ normalisation + epilogue (128 threads)
+    // tcgen05.ld / tcgen05.st are warp-collective and the epilogue barriers take all four warps:
+    // every branch below is uniform over the four warps (their exits agree through epi_sync_and).
     const int q = warp & 3;
     const int r = q * 32 + lane;               // row within the tile == TMEM lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    int cur_m = -1, seg = 0, acc = 0;
+    const bool leader = threadIdx.x == 64;     // issues the TMA stores
+    int cur_m = -1, seg = 0, acc = 0, n_out = 0;
     uint32_t acc_phase = 0;
+    bool ok = true;
     for (int u = u_begin; u < u_end; ++u) {
-      const int m = u / p.H, h = u % p.H;
+      const int m = u / (2 * p.H), h = (u >> 1) % p.H, half = u & 1;
+      const int b = m / p.mt_per_b, t0 = (m % p.mt_per_b) * BM;
       if (m != cur_m) {
-        if (!mbar_wait(&a_full, seg & 1, abort_p)) break;
-        // RMSNorm of row r, in place in the swizzled A tile: logical 16-byte chunk c of a 128-byte
-        // row sits at chunk position c ^ (r & 7). Sum of squares in ascending feature order.
-        uint8_t* row_base = sA + r * 128;
-        float ss = 0.f;
-#pragma unroll 1
-        for (int a = 0; a < NKATOM; ++a) {
+        // RMSNorm of row (b, t0 + r) into TMEM once the previous tile's MMAs are done with y
+        if (seg > 0) ok = __all_sync(0xffffffffu, mbar_wait(&a_free, (seg - 1) & 1, abort_p));
+        ok = epi_sync_and(ok);
+        if (!ok) break;
+        tc_fence_after();
+        const int t = t0 + r;
+        const bool valid = t < p.T;
+        const uint4* row = reinterpret_cast<const uint4*>(p.c_kv + (static_cast<int64_t>(b) * p.T + (valid ? t : 0)) * KDIM);
+        float ss = 0.f;   // sum of squares in ascending feature order
+#pragma unroll 4
+        for (int a = 0; a < KDIM / 8; ++a) {
+          const uint4 v = valid ? __ldg(row + a) : make_uint4(0, 0, 0, 0);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 v = *reinterpret_cast<const uint4*>(row_base + a * A_ATOM_BYTES + ((c ^ (r & 7)) * 16));
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float lo = __uint_as_float(w[e] << 16);
-              const float hi = __uint_as_float(w[e] & 0xFFFF0000u);
-              ss = __fadd_rn(ss, __fmul_rn(lo, lo));
-              ss = __fadd_rn(ss, __fmul_rn(hi, hi));
-            }
+          for (int e = 0; e < 4; ++e) {
+            const float lo = __uint_as_float(w[e] << 16);
+            const float hi = __uint_as_float(w[e] & 0xFFFF0000u);
+            ss = __fadd_rn(ss, __fmul_rn(lo, lo));
+            ss = __fadd_rn(ss, __fmul_rn(hi, hi));
           }
         }
         const float var = __fmul_rn(ss, 1.0f / KDIM);   // exact: division by a power of two
         const float rinv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, RMS_EPS)));
 #pragma unroll 1
-        for (int a = 0; a < NKATOM; ++a) {
+        for (int cc = 0; cc < KDIM / 64; ++cc) {   // 64 features -> 32 TMEM columns
+          uint32_t o[32];
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint4* ptr = reinterpret_cast<uint4*>(row_base + a * A_ATOM_BYTES + c * 16);
-            const uint4 v = *ptr;
-            const int col0 = a * KATOM + ((c ^ (r & 7)) * 8);
-            const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma + col0));
-            const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma + col0 + 4));
+          for (int a = 0; a < 8; ++a) {
+            const uint4 v = valid ? __ldg(row + cc * 8 + a) : make_uint4(0, 0, 0, 0);
+            const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma + cc * 64 + a * 8));
+            const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma + cc * 64 + a * 8 + 4));
             const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            uint32_t o[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float lo = __uint_as_float(w[e] << 16);
               const float hi = __uint_as_float(w[e] & 0xFFFF0000u);
-              o[e] = pack_bf16x2(__fmul_rn(g[2 * e], __fmul_rn(lo, rinv)), __fmul_rn(g[2 * e + 1], __fmul_rn(hi, rinv)));
+              o[a * 4 + e] = pack_bf16x2(__fmul_rn(g[2 * e], __fmul_rn(lo, rinv)), __fmul_rn(g[2 * e + 1], __fmul_rn(hi, rinv)));
             }
-            *ptr = make_uint4(o[0], o[1], o[2], o[3]);
           }
+          tmem_st_32x32b_x32(lane_addr + TM_A + static_cast<uint32_t>(cc * 32), o);
         }
-        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();
         mbar_arrive(&a_ready);
         cur_m = m;
         ++seg;
       }
-      if (!mbar_wait(&acc_full[acc], acc_phase, abort_p)) break;
-      tc_fence_after();
-      const int row_g = m * BM + r;
-      const bool valid = row_g < p.M;
-      uint16_t* dst = nullptr;
-      uint8_t* dlo = nullptr;
-      if (valid) {
-        const int b = row_g / p.T, t = row_g % p.T;
-        const int64_t prow = (static_cast<int64_t>(b) * p.H + h) * p.T + t;
-        dst = p.kv + prow * BN;
-        dlo = p.klo + prow * 128;
-      }
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(lane_addr + static_cast<uint32_t>(acc * BN + c0), v);
+
+      // accumulator -> registers, then the accumulator is free for the unit after next
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&acc_full[acc], acc_phase, abort_p));
+      uint32_t v[BN];
+      if (got) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c)
+          tmem_ld_32x32b_x32(lane_addr + TM_ACC + static_cast<uint32_t>(acc * BN + c * 32),
+                             *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
         tmem_ld_wait();
-        if (valid) {
-          uint32_t hw[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) hw[i] = pack_f16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(hw[4 * i], hw[4 * i + 1], hw[4 * i + 2], hw[4 * i + 3]);
-          if (c0 < 128) {
-            // residual of k_nope after the fp16 rounding, scaled by 2^11, as e4m3
-            uint32_t lw[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              float rr[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int k = 4 * i + e;
-                const uint16_t hb = static_cast<uint16_t>((hw[k >> 1] >> ((k & 1) * 16)) & 0xFFFFu);
-                rr[e] = __fmul_rn(__fsub_rn(__uint_as_float(v[k]), f16_bits_to_float(hb)), KLO_SCALE);
-              }
-              lw[i] = static_cast<uint32_t>(pack_e4m3x2(rr[0], rr[1])) | (static_cast<uint32_t>(pack_e4m3x2(rr[2], rr[3])) << 16);
-            }
-            uint4* l4 = reinterpret_cast<uint4*>(dlo + c0);
-            l4[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            l4[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
-          }
-        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[acc]);
       }
-      tc_fence_before();
-      mbar_arrive(&acc_empty[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
+      // staging buffer n_out & 1 is free once the stores of two units ago have read it
+      if (leader) tma_store_wait_read<1>();
+      ok = epi_sync_and(got);
+      if (!ok) break;
+      uint8_t* so = sOut + (n_out & 1) * OUT_STAGE_BYTES;
+      // kv: 128 fp16 columns = 16 chunks of 16 bytes; chunk c of row r at atom c / 8, position
+      // (c % 8) ^ (r & 7) (the 128-byte swizzle the tensor map expects)
+      uint32_t hw[BN / 2];
+#pragma unroll
+      for (int i = 0; i < BN / 2; ++i) hw[i] = pack_f16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        *reinterpret_cast<uint4*>(so + (c >> 3) * OUT_ATOM + r * 128 + (((c & 7) ^ (r & 7)) * 16)) =
+            make_uint4(hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
+      if (half == 0) {
+        // residual of k_nope after the fp16 rounding, scaled by 2^11, as e4m3: 8 chunks of 16 bytes
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t lw[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float rr[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int k = c * 16 + i * 4 + e;
+              const uint16_t hb = static_cast<uint16_t>((hw[k >> 1] >> ((k & 1) * 16)) & 0xFFFFu);
+              rr[e] = __fmul_rn(__fsub_rn(__uint_as_float(v[k]), f16_bits_to_float(hb)), KLO_SCALE);
+            }
+            lw[i] = static_cast<uint32_t>(pack_e4m3x2(rr[0], rr[1])) | (static_cast<uint32_t>(pack_e4m3x2(rr[2], rr[3])) << 16);
+          }
+          *reinterpret_cast<uint4*>(so + 2 * OUT_ATOM + r * 128 + ((c ^ (r & 7)) * 16)) =
+              make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      named_sync(EPI_BAR, 128);
+      if (leader) {
+        const int plane = b * p.H + h;
+        tma_store_3d(&tm_kv, so, half * BN, t0, plane);
+        tma_store_3d(&tm_kv, so + OUT_ATOM, half * BN + 64, t0, plane);
+        if (half == 0) tma_store_3d(&tm_klo, so + 2 * OUT_ATOM, 0, t0, plane);
+        tma_store_commit();
+      }
+      ++n_out;
     }
+    // the stores read shared memory until they complete: wait before the CTA exits
+    if (leader) tma_store_wait_all<0>();
   }
 
   tc_fence_before();

@@ -84,30 +84,37 @@ mla_status launch_canon(const int32_t* topk_idx, mla_dims d, uint32_t* sel_bits,
 
 mla_status launch_kvnorm_wkvb(const mla_bf16* c_kv, const float* gamma, const mla_bf16* wkv_b, mla_dims d,
                               uint16_t* kv, uint8_t* klo, int num_sms, cudaStream_t st) {
-  const int M = d.B * d.T;
-  CUtensorMap tm_ckv, tm_w;
-  {
-    const uint64_t dims[2] = {kLatent, static_cast<uint64_t>(M)};
-    const uint64_t strides[1] = {kLatent * 2};
-    const uint32_t box[2] = {64, mla::k1::BM};
-    if (!mla::make_tmap_bf16(&tm_ckv, c_kv, 2, dims, strides, box)) return MLA_ERR_CUDA;
-  }
+  CUtensorMap tm_w, tm_kv, tm_klo;
   {
     const uint64_t dims[2] = {kLatent, static_cast<uint64_t>(d.H) * kKV};
     const uint64_t strides[1] = {kLatent * 2};
     const uint32_t box[2] = {64, mla::k1::BN};
     if (!mla::make_tmap_bf16(&tm_w, wkv_b, 2, dims, strides, box)) return MLA_ERR_CUDA;
   }
+  {  // output kv [B*H planes][T][256] fp16, stored in 64-column x 128-row boxes
+    const uint64_t dims[3] = {kKV, static_cast<uint64_t>(d.T), static_cast<uint64_t>(d.B) * d.H};
+    const uint64_t strides[2] = {kKV * 2, static_cast<uint64_t>(d.T) * kKV * 2};
+    const uint32_t box[3] = {64, mla::k1::BM, 1};
+    if (!mla::make_tmap_f16(&tm_kv, kv, 3, dims, strides, box)) return MLA_ERR_CUDA;
+  }
+  {  // output klo [B*H planes][T][128] bytes, stored in 128-column x 128-row boxes
+    const uint64_t dims[3] = {128, static_cast<uint64_t>(d.T), static_cast<uint64_t>(d.B) * d.H};
+    const uint64_t strides[2] = {128, static_cast<uint64_t>(d.T) * 128};
+    const uint32_t box[3] = {128, mla::k1::BM, 1};
+    if (!mla::make_tmap_u8(&tm_klo, klo, 3, dims, strides, box)) return MLA_ERR_CUDA;
+  }
   mla::k1::Params p;
-  p.M = M;
+  p.B = d.B;
   p.T = d.T;
   p.H = d.H;
-  p.units = (M + mla::k1::BM - 1) / mla::k1::BM * d.H;
+  p.mt_per_b = (d.T + mla::k1::BM - 1) / mla::k1::BM;
+  const int64_t units = static_cast<int64_t>(d.B) * p.mt_per_b * d.H * 2;
+  if (units > INT32_MAX / 2) return MLA_ERR_UNSUPPORTED;
+  p.units = static_cast<int>(units);
+  p.c_kv = c_kv;
   p.gamma = gamma;
-  p.kv = kv;
-  p.klo = klo;
   const int grid = p.units < num_sms ? p.units : num_sms;
-  mla::k1::kvnorm_wkvb_kernel<<<grid, mla::k1::THREADS, mla::k1::SMEM_BYTES, st>>>(tm_ckv, tm_w, p);
+  mla::k1::kvnorm_wkvb_kernel<<<grid, mla::k1::THREADS, mla::k1::SMEM_BYTES, st>>>(tm_w, tm_kv, tm_klo, p);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
