@@ -46,6 +46,38 @@ def measured_peaks():
     return 1800.0, 1400.0, 6400.0, "fallback"
 
 
+def kernel_sources_sha256() -> str:
+    """sha256 over libmla's kernel sources and header (the inputs of every kernel build)."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_latent_attention_norm_b300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    with open(os.path.join(ROOT, "include", "mla.h"), "rb") as fh:
+        h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes (read + write) per launch of the attention kernel, from the committed ncu
+    summary of the headline workload, or None when that capture predates the current sources."""
+    if workload != "headline":
+        return None
+    path = os.path.join(ROOT, "profiles", "kernels_headline_full.md")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            if line.startswith("traffic: "):
+                kv = dict(x.split("=", 1) for x in line.split()[1:] if "=" in x)
+                if kv.get("kernel") == "sparse_attn_kernel" and kv.get("sources_sha256") == kernel_sources_sha256():
+                    return int(kv["dram_bytes_per_launch"])
+    return None
+
+
 def dist_setup():
     """Under torchrun (WORLD_SIZE > 1) every rank runs an independent replica of the workload."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -341,7 +373,8 @@ def run_ours(args, rank, world, dist):
         "kernel_ms": {"sparse_attn": attn_avg, "kvnorm_wkvb": gemm_avg, "canon_select": canon_avg},
         "kvnorm_wkvb_tflops": up_flops / (gemm_avg / 1e3) / 1e12,
         "roofline": {"kernel": "sparse_attn_kernel", "bound": "tensor", "achieved": achieved, "peak": peak_burst,
-                     "unit": "TFLOP/s", "frac": achieved / peak_burst, "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / peak_burst, "traffic": profiled_traffic(w.name),
+                     "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                      "peak_kind": f"{peak_kind} bf16 burst",
                      "algorithmic": "2*H*sum_n*(192+128) flops per launch"},
         "cpu_baseline": cpu_baseline(host, w),

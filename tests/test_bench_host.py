@@ -57,3 +57,19 @@ def test_max_over_ranks_gloo_world2():
         assert p.exitcode == 0
     got = dict(q.get(timeout=10) for _ in range(2))
     assert got == {0: 3.5, 1: 3.5}
+
+
+def test_profiled_traffic_tracks_kernel_sources(tmp_path, monkeypatch):
+    # the committed headline capture is reported only while the kernel sources are the ones it
+    # measured; another workload or a changed source hash gives None
+    assert bench.profiled_traffic("tiny") is None
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "kernels_headline_full.md").write_text(
+        "x\ntraffic: kernel=sparse_attn_kernel dram_bytes_per_launch=123 sources_sha256=%s\n" % bench.kernel_sources_sha256())
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_sources_sha256", lambda: "0" * 64)
+    assert bench.profiled_traffic("headline") is None
+    (prof / "kernels_headline_full.md").write_text(
+        "traffic: kernel=sparse_attn_kernel dram_bytes_per_launch=123 sources_sha256=%s\n" % ("0" * 64))
+    assert bench.profiled_traffic("headline") == 123
