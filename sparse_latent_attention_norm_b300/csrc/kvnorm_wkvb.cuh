@@ -19,12 +19,13 @@
 // unit is one row tile x one half of one head (k_nope: W rows h*256 + [0,128), or v: h*256 +
 // [128,256)) x the whole latent (512). The normalised row tile y (128 x 512 bf16) lives in TMEM
 // (256 columns, bf16 pairs) as the A operand of every unit of the tile; W streams through a
-// 6-stage TMA ring of 128 x 64 slices (B operand), and each unit is 32 UMMAs M=128 N=128 K=16
+// 8-stage TMA ring of 128 x 64 slices (B operand), and each unit is 32 UMMAs M=128 N=128 K=16
 // into one of two TMEM accumulators, so a unit's epilogue overlaps the next unit's MMAs. The
 // epilogue converts the accumulator, writes it 128-byte-swizzled into one of two shared staging
 // buffers and TMA-stores it (kv: two 64-column boxes, klo: one box); rows past T are clipped by
-// the tensor map. A CTA takes a contiguous range of units, row-tile-major, so it normalises at
-// most a few row tiles.
+// the tensor map. The two CTAs of a cluster take adjacent row tiles and walk the same units; each
+// loads half of every W slice and multicasts it to both, so W leaves L2 once per cluster. A
+// cluster takes a contiguous range of units, row-tile-major, so it normalises few row tiles.
 //
 // Warp roles (192 threads): warp 0 TMA producer of W, warp 1 TMEM owner + MMA issuer, warps 2-5
 // normalise rows into TMEM and run the epilogue (warp w owns TMEM lanes 32*(w%4) .. +31).
@@ -41,11 +42,14 @@ constexpr int KDIM = 512;                       // kv_lora_rank
 constexpr int KATOM = 64;                       // bf16 elements per 128-byte swizzle row
 constexpr int NKATOM = KDIM / KATOM;            // 8
 constexpr int B_STAGE_BYTES = BN * 128;         // 16 KB: 128 W rows x 64 latent features
-constexpr int NSTAGE = 6;
+constexpr int NSTAGE = 8;
 constexpr int OUT_ATOM = BM * 128;              // 16 KB: 128 rows x 128 bytes, 128-byte swizzle
 constexpr int OUT_STAGE_BYTES = 3 * OUT_ATOM;   // kv: two atoms (128 fp16 columns); klo: one atom
 constexpr int NOUT = 2;
 constexpr int THREADS = 192;
+constexpr int CLUSTER = 2;                      // CTAs per cluster sharing every W slice
+constexpr int B_ROWS_PER_CTA = BN / CLUSTER;    // W rows each CTA of a cluster loads per slice
+constexpr uint16_t CLUSTER_MASK = (1u << CLUSTER) - 1;
 constexpr int TILE_BYTES = NSTAGE * B_STAGE_BYTES + NOUT * OUT_STAGE_BYTES;
 
 // Barriers after the tiles in the dynamic shared memory (no static shared memory: the dynamic
@@ -69,7 +73,8 @@ constexpr int EPI_BAR = 1;             // named barrier of the four epilogue war
 struct Params {
   int B, T, H;
   int mt_per_b;            // row tiles per batch: ceil(T / 128)
-  int units;               // B * mt_per_b * H * 2
+  int n_mtiles;            // B * mt_per_b
+  int units;               // ceil(n_mtiles / CLUSTER) * H * 2: units of a cluster
   const uint16_t* c_kv;    // [B, T, 512] bf16
   const float* gamma;      // [512]
 };
@@ -86,7 +91,7 @@ __device__ __forceinline__ bool epi_sync_and(bool pred) {
   return r != 0;
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
     kvnorm_wkvb_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_kv,
                        const __grid_constant__ CUtensorMap tm_klo, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -109,10 +114,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = warp_id();
   const int lane = lane_id();
 
-  // contiguous range of units for this CTA: u -> row tile m = u / (2H), head (u / 2) % H, half u % 2
-  const int G = gridDim.x;
-  const int u_begin = static_cast<int>((static_cast<int64_t>(p.units) * blockIdx.x) / G);
-  const int u_end = static_cast<int>((static_cast<int64_t>(p.units) * (blockIdx.x + 1)) / G);
+  // The CTAs of a cluster take adjacent row tiles and walk the same units (head, half), so each W
+  // slice is read from L2 once per cluster: every CTA loads 1/CLUSTER of its rows and multicasts
+  // them to the whole cluster. Contiguous range of cluster units: u -> row-tile group u / (2H),
+  // head (u / 2) % H, half u % 2; this CTA's row tile is group * CLUSTER + rank.
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int G = gridDim.x / CLUSTER;
+  const int cl = blockIdx.x / CLUSTER;
+  const int u_begin = static_cast<int>((static_cast<int64_t>(p.units) * cl) / G);
+  const int u_end = static_cast<int>((static_cast<int64_t>(p.units) * (cl + 1)) / G);
 
   if (threadIdx.x == 0) {
     ctl.abort_flag = 0;
@@ -120,8 +130,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&a_ready, 128);
     mbar_init(&drain, 1);
     for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(&b_full[s], 1);
-      mbar_init(&b_empty[s], 1);
+      mbar_init(&b_full[s], 1);              // own producer's expect_tx; bytes from every CTA's part
+      mbar_init(&b_empty[s], CLUSTER);       // one commit from each CTA's MMA issuer
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&acc_full[s], 1);
@@ -141,10 +151,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // every CTA's barriers are initialised before any multicast copy or commit reaches them
+  cluster_sync_all();
   const uint32_t tmem = ctl.tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer: W slices
+    // ------------------------------------------------ TMA producer: this CTA's part of every W slice
+    // A slice stage is refilled once every CTA of the cluster has consumed it (b_empty counts
+    // one commit per CTA); the own b_full expects the whole slice, whose parts arrive from all.
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -156,7 +170,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int ka = 0; ka < NKATOM; ++ka) {
           if (!mbar_wait(&b_empty[stage], phase ^ 1, abort_p)) { ok = false; break; }
           mbar_arrive_expect_tx(&b_full[stage], B_STAGE_BYTES);
-          tma_load_2d(sB + stage * B_STAGE_BYTES, &tm_w, &b_full[stage], ka * KATOM, h * 256 + half * BN);
+          tma_load_2d_multicast(sB + stage * B_STAGE_BYTES + rank * B_ROWS_PER_CTA * 128, &tm_w, &b_full[stage],
+                                ka * KATOM, h * 256 + half * BN + rank * B_ROWS_PER_CTA, CLUSTER_MASK);
           pending[stage] = true;
           pend_parity[stage] = phase;
           if (++stage == NSTAGE) { stage = 0; phase ^= 1; }
@@ -199,7 +214,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             umma_ts(d, tmem + TM_A + static_cast<uint32_t>((ka * 4 + k4) * 8), db + k4 * 2, idesc,
                     (ka | k4) != 0 ? 1u : 0u);
           issued = true;
-          umma_commit(&b_empty[stage]);
+          umma_commit_multicast(&b_empty[stage], CLUSTER_MASK);
           if (++stage == NSTAGE) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -225,8 +240,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int u = u_begin; u < u_end; ++u) {
-      const int m = u / (2 * p.H), h = (u >> 1) % p.H, half = u & 1;
-      const int b = m / p.mt_per_b, t0 = (m % p.mt_per_b) * BM;
+      const int m = (u / (2 * p.H)) * CLUSTER + rank, h = (u >> 1) % p.H, half = u & 1;
+      const bool active = m < p.n_mtiles;   // the last group may have fewer row tiles than CTAs
+      const int b = active ? m / p.mt_per_b : 0, t0 = active ? (m % p.mt_per_b) * BM : 0;
       if (m != cur_m) {
         // RMSNorm of row (b, t0 + r) into TMEM once the previous tile's MMAs are done with y
         if (seg > 0) ok = __all_sync(0xffffffffu, mbar_wait(&a_free, (seg - 1) & 1, abort_p));
@@ -234,7 +250,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!ok) break;
         tc_fence_after();
         const int t = t0 + r;
-        const bool valid = t < p.T;
+        const bool valid = active && t < p.T;
         const uint4* row = reinterpret_cast<const uint4*>(p.c_kv + (static_cast<int64_t>(b) * p.T + (valid ? t : 0)) * KDIM);
         float ss = 0.f;   // sum of squares in ascending feature order
 #pragma unroll 4
@@ -328,7 +344,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       fence_proxy_async_smem();
       named_sync(EPI_BAR, 128);
-      if (leader) {
+      if (leader && active) {
         const int plane = b * p.H + h;
         tma_store_3d(&tm_kv, so, half * BN, t0, plane);
         tma_store_3d(&tm_kv, so + OUT_ATOM, half * BN + 64, t0, plane);
@@ -347,6 +363,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
+  // no CTA leaves while another CTA's multicast commits may still arrive on its barriers
+  cluster_sync_all();
 }
 
 }  // namespace k1

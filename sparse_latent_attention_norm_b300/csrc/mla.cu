@@ -26,11 +26,12 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   bool ready = false;
   int num_sms = 0;
+  int k1_clusters = 0;   // clusters of the GEMM stage that fit on the device at once (0: unknown)
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
 
-mla_status device_setup(int* num_sms) {
+mla_status device_setup(int* num_sms, int* k1_clusters) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_dev_mutex);
@@ -43,9 +44,24 @@ mla_status device_setup(int* num_sms) {
     if (cudaFuncSetAttribute(mla::k2::sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              mla::k2::SMEM_BYTES) != cudaSuccess)
       return MLA_ERR_CUDA;
+    {
+      // the GEMM stage's grid is a fixed set of clusters with fixed unit ranges: launch no more
+      // clusters than can be resident together
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(d.num_sms / mla::k1::CLUSTER * mla::k1::CLUSTER));
+      cfg.blockDim = dim3(mla::k1::THREADS);
+      cfg.dynamicSmemBytes = mla::k1::SMEM_BYTES;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, mla::k1::kvnorm_wkvb_kernel, &cfg) != cudaSuccess) {
+        n = 0;
+        (void)cudaGetLastError();   // the query's error is not the caller's
+      }
+      d.k1_clusters = n;
+    }
     d.ready = true;
   }
   *num_sms = d.num_sms;
+  if (k1_clusters) *k1_clusters = d.k1_clusters;
   return MLA_OK;
 }
 
@@ -83,12 +99,12 @@ mla_status launch_canon(const int32_t* topk_idx, mla_dims d, uint32_t* sel_bits,
 }
 
 mla_status launch_kvnorm_wkvb(const mla_bf16* c_kv, const float* gamma, const mla_bf16* wkv_b, mla_dims d,
-                              uint16_t* kv, uint8_t* klo, int num_sms, cudaStream_t st) {
+                              uint16_t* kv, uint8_t* klo, int num_sms, int k1_max_clusters, cudaStream_t st) {
   CUtensorMap tm_w, tm_kv, tm_klo;
   {
     const uint64_t dims[2] = {kLatent, static_cast<uint64_t>(d.H) * kKV};
     const uint64_t strides[1] = {kLatent * 2};
-    const uint32_t box[2] = {64, mla::k1::BN};
+    const uint32_t box[2] = {64, mla::k1::B_ROWS_PER_CTA};
     if (!mla::make_tmap_bf16(&tm_w, wkv_b, 2, dims, strides, box)) return MLA_ERR_CUDA;
   }
   {  // output kv [B*H planes][T][256] fp16, stored in 64-column x 128-row boxes
@@ -108,12 +124,17 @@ mla_status launch_kvnorm_wkvb(const mla_bf16* c_kv, const float* gamma, const ml
   p.T = d.T;
   p.H = d.H;
   p.mt_per_b = (d.T + mla::k1::BM - 1) / mla::k1::BM;
-  const int64_t units = static_cast<int64_t>(d.B) * p.mt_per_b * d.H * 2;
+  const int64_t n_mtiles = static_cast<int64_t>(d.B) * p.mt_per_b;
+  const int64_t units = (n_mtiles + mla::k1::CLUSTER - 1) / mla::k1::CLUSTER * d.H * 2;
   if (units > INT32_MAX / 2) return MLA_ERR_UNSUPPORTED;
+  p.n_mtiles = static_cast<int>(n_mtiles);
   p.units = static_cast<int>(units);
   p.c_kv = c_kv;
   p.gamma = gamma;
-  const int grid = p.units < num_sms ? p.units : num_sms;
+  // whole clusters, no more than can be resident at once (each cluster's range of units is fixed)
+  int clusters = k1_max_clusters > 0 ? k1_max_clusters : num_sms / mla::k1::CLUSTER;
+  if (clusters > p.units) clusters = p.units;
+  const int grid = clusters * mla::k1::CLUSTER;
   mla::k1::kvnorm_wkvb_kernel<<<grid, mla::k1::THREADS, mla::k1::SMEM_BYTES, st>>>(tm_w, tm_kv, tm_klo, p);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
@@ -223,8 +244,8 @@ mla_status mla_canon_select(const int32_t* topk_idx, mla_dims d, uint32_t* sel_b
   if (s != MLA_OK) return s;
   if (!topk_idx || !sel_bits || !aligned16(topk_idx) || !aligned16(sel_bits)) return MLA_ERR_INVALID_ARG;
   if (n_keys && (reinterpret_cast<uintptr_t>(n_keys) & 3u)) return MLA_ERR_INVALID_ARG;
-  int sms;
-  if ((s = device_setup(&sms)) != MLA_OK) return s;
+  int sms, k1_clusters;
+  if ((s = device_setup(&sms, &k1_clusters)) != MLA_OK) return s;
   return launch_canon(topk_idx, d, sel_bits, n_keys, flags, nullptr, as_stream(stream));
 }
 
@@ -235,9 +256,9 @@ mla_status mla_kvnorm_wkvb(const mla_bf16* c_kv, const float* gamma, const mla_b
   if (!c_kv || !gamma || !wkv_b || !kv || !klo) return MLA_ERR_INVALID_ARG;
   if (!aligned16(c_kv) || !aligned16(gamma) || !aligned16(wkv_b) || !aligned16(kv) || !aligned16(klo))
     return MLA_ERR_INVALID_ARG;
-  int sms;
-  if ((s = device_setup(&sms)) != MLA_OK) return s;
-  return launch_kvnorm_wkvb(c_kv, gamma, wkv_b, d, kv, klo, sms, as_stream(stream));
+  int sms, k1_clusters;
+  if ((s = device_setup(&sms, &k1_clusters)) != MLA_OK) return s;
+  return launch_kvnorm_wkvb(c_kv, gamma, wkv_b, d, kv, klo, sms, k1_clusters, as_stream(stream));
 }
 
 mla_status mla_sparse_attention(const mla_bf16* q, const mla_bf16* k_pe, const uint16_t* kv, const uint8_t* klo,
@@ -248,8 +269,8 @@ mla_status mla_sparse_attention(const mla_bf16* q, const mla_bf16* k_pe, const u
   if (!aligned16(q) || !aligned16(k_pe) || !aligned16(kv) || !aligned16(klo) || !aligned16(sel_bits) ||
       !aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u))
     return MLA_ERR_INVALID_ARG;
-  int sms;
-  if ((s = device_setup(&sms)) != MLA_OK) return s;
+  int sms, k1_clusters;
+  if ((s = device_setup(&sms, &k1_clusters)) != MLA_OK) return s;
   uint32_t* sched = nullptr;
   if ((s = staged_sched_counter(&sched)) != MLA_OK) return s;
   if (cudaMemsetAsync(sched, 0, sizeof(uint32_t), as_stream(stream)) != cudaSuccess) return MLA_ERR_CUDA;
@@ -272,8 +293,8 @@ mla_status mla_sparse_prefill_ex(const mla_bf16* q, const mla_bf16* c_kv, const 
   if (workspace != nullptr) {
     if ((reinterpret_cast<uintptr_t>(workspace) & 1023u) || workspace_bytes < need) return MLA_ERR_WORKSPACE;
   }
-  int sms;
-  if ((s = device_setup(&sms)) != MLA_OK) return s;
+  int sms, k1_clusters;
+  if ((s = device_setup(&sms, &k1_clusters)) != MLA_OK) return s;
   cudaStream_t st = as_stream(stream);
   void* ws = workspace;
   bool owned = false;
@@ -287,7 +308,7 @@ mla_status mla_sparse_prefill_ex(const mla_bf16* q, const mla_bf16* c_kv, const 
   uint32_t* bits = reinterpret_cast<uint32_t*>(klo + align_up(klo_bytes(d), 1024));
   uint32_t* sched = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(bits) + align_up(bits_bytes(d), 1024));
   s = launch_canon(topk_idx, d, bits, n_keys, flags, sched, st);
-  if (s == MLA_OK) s = launch_kvnorm_wkvb(c_kv, gamma, wkv_b, d, kv, klo, sms, st);
+  if (s == MLA_OK) s = launch_kvnorm_wkvb(c_kv, gamma, wkv_b, d, kv, klo, sms, k1_clusters, st);
   if (s == MLA_OK) s = launch_sparse_attn(q, k_pe, kv, klo, bits, out, lse, d, sched, sms, st);
   if (owned && cudaFreeAsync(ws, st) != cudaSuccess && s == MLA_OK) s = MLA_ERR_CUDA;
   return s;
@@ -344,8 +365,8 @@ mla_status mla_sparse_prefill_noalloc(const mla_bf16* q, const mla_bf16* c_kv, c
       !aligned16(topk_idx) || !aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u))
     return MLA_ERR_INVALID_ARG;
   if (mla_sparse_prefill_workspace_size(d) > static_cast<size_t>(MLA_NOALLOC_SCRATCH_BYTES)) return MLA_ERR_WORKSPACE;
-  int sms;
-  if ((s = device_setup(&sms)) != MLA_OK) return s;
+  int sms, k1_clusters;
+  if ((s = device_setup(&sms, &k1_clusters)) != MLA_OK) return s;
   void* scratch = nullptr;
   if ((s = noalloc_scratch_address(&scratch)) != MLA_OK) return s;
   // Same carve as mla_sparse_prefill_ex. The only word that has to start at zero, the attention
@@ -358,7 +379,7 @@ mla_status mla_sparse_prefill_noalloc(const mla_bf16* q, const mla_bf16* c_kv, c
   uint32_t* bits = reinterpret_cast<uint32_t*>(klo + align_up(klo_bytes(d), 1024));
   uint32_t* sched = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(bits) + align_up(bits_bytes(d), 1024));
   s = launch_canon(topk_idx, d, bits, nullptr, 0u, sched, st);
-  if (s == MLA_OK) s = launch_kvnorm_wkvb(c_kv, gamma, wkv_b, d, kv, klo, sms, st);
+  if (s == MLA_OK) s = launch_kvnorm_wkvb(c_kv, gamma, wkv_b, d, kv, klo, sms, k1_clusters, st);
   if (s == MLA_OK) s = launch_sparse_attn(q, k_pe, kv, klo, bits, out, lse, d, sched, sms, st);
   return s;
 }
