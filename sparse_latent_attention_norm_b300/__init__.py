@@ -262,3 +262,93 @@ class HostPrefill:
             self.lse_h.copy_(self.lse, non_blocking=True)
         s.synchronize()
         return self.out_h, self.lse_h
+
+
+class HostPrefillPipeline:
+    """Pipelined end-to-end use from host memory. Each submitted step copies its inputs from
+    (pinned) host tensors to the device, runs mla_sparse_prefill and copies out / lse back to
+    pinned host tensors, like HostPrefill, but on three streams: the host->device copies of step
+    i run while step i-1 computes and step i-2's results travel back. Device input and output
+    buffers are double-buffered (`depth` sets); the steps compute in submission order on one
+    stream and share one workspace.
+
+        pipe = HostPrefillPipeline(B, T, H, K)
+        h = pipe.submit(inputs)          # returns at once
+        out, lse = pipe.result(h)        # waits for that step's results on the host
+
+    The host tensors a step returns are reused `depth` submissions later."""
+
+    def __init__(self, B: int, T: int, H: int, K: int, device="cuda", depth: int = 2):
+        import torch
+        if depth < 1:
+            raise ValueError("depth must be >= 1")
+        self.depth = depth
+        self.dev = torch.device(device)
+        self.slots = []
+        for _ in range(depth):
+            d = {
+                "q": torch.empty((B, T, H, QK), dtype=torch.bfloat16, device=self.dev),
+                "c_kv": torch.empty((B, T, LATENT), dtype=torch.bfloat16, device=self.dev),
+                "k_pe": torch.empty((B, T, ROPE), dtype=torch.bfloat16, device=self.dev),
+                "gamma": torch.empty((LATENT,), dtype=torch.float32, device=self.dev),
+                "wkv_b": torch.empty((H * (NOPE + V), LATENT), dtype=torch.bfloat16, device=self.dev),
+                "topk_idx": torch.empty((B, T, K), dtype=torch.int32, device=self.dev),
+            }
+            self.slots.append({
+                "in": d,
+                "out": torch.empty((B, T, H, V), dtype=torch.bfloat16, device=self.dev),
+                "lse": torch.empty((B, T, H), dtype=torch.float32, device=self.dev),
+                "out_h": torch.empty((B, T, H, V), dtype=torch.bfloat16, pin_memory=True),
+                "lse_h": torch.empty((B, T, H), dtype=torch.float32, pin_memory=True),
+                "in_free": None,    # event: the step that last used this slot has read its inputs
+                "out_free": None,   # event: that step's results have reached the host
+            })
+        self.ws = alloc_workspace(B, T, H, K, device=self.dev)
+        self.s_h2d = torch.cuda.Stream(device=self.dev)
+        self.s_comp = torch.cuda.Stream(device=self.dev)
+        self.s_d2h = torch.cuda.Stream(device=self.dev)
+        self.n = 0
+
+    def h2d_bytes(self, inputs) -> int:
+        return sum(inputs[k].numel() * inputs[k].element_size() for k in self.slots[0]["in"])
+
+    def d2h_bytes(self) -> int:
+        o = self.slots[0]
+        return o["out"].numel() * 2 + o["lse"].numel() * 4
+
+    def submit(self, inputs):
+        """Enqueue one step (inputs: dict of host tensors, pinned for asynchronous copies). Returns
+        a handle for result()."""
+        import torch
+        slot = self.slots[self.n % self.depth]
+        self.n += 1
+        if slot["in_free"] is not None:
+            self.s_h2d.wait_event(slot["in_free"])
+        with torch.cuda.stream(self.s_h2d):
+            for k, dst in slot["in"].items():
+                dst.copy_(inputs[k], non_blocking=True)
+        copied = torch.cuda.Event()
+        copied.record(self.s_h2d)
+        self.s_comp.wait_event(copied)
+        if slot["out_free"] is not None:
+            self.s_comp.wait_event(slot["out_free"])
+        d = slot["in"]
+        sparse_prefill(d["q"], d["c_kv"], d["k_pe"], d["gamma"], d["wkv_b"], d["topk_idx"], out=slot["out"],
+                       lse=slot["lse"], workspace=self.ws, stream=self.s_comp)
+        computed = torch.cuda.Event()
+        computed.record(self.s_comp)
+        slot["in_free"] = computed
+        self.s_d2h.wait_event(computed)
+        with torch.cuda.stream(self.s_d2h):
+            slot["out_h"].copy_(slot["out"], non_blocking=True)
+            slot["lse_h"].copy_(slot["lse"], non_blocking=True)
+        back = torch.cuda.Event()
+        back.record(self.s_d2h)
+        slot["out_free"] = back
+        return (slot, back)
+
+    def result(self, handle):
+        """Host (out, lse) of a submitted step, once it has arrived."""
+        slot, back = handle
+        back.synchronize()
+        return slot["out_h"], slot["lse_h"]

@@ -531,8 +531,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t v[PCOLS];
             tmem_ld_32x32b_x32(tmem + lane_off + TM_S + static_cast<uint32_t>(sb * BK + part * PCOLS), v);
             tmem_ld_wait();
+            if (__all_sync(0xffffffffu, mask == 0xFFFFFFFFu)) {   // every key of the part selected
 #pragma unroll
-            for (int e = 0; e < PCOLS; ++e) s[e] = ((mask >> e) & 1u) ? __uint_as_float(v[e]) : -INFINITY;
+              for (int e = 0; e < PCOLS; ++e) s[e] = __uint_as_float(v[e]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < PCOLS; ++e) s[e] = ((mask >> e) & 1u) ? __uint_as_float(v[e]) : -INFINITY;
+            }
           } else {
 #pragma unroll
             for (int e = 0; e < PCOLS; ++e) s[e] = -INFINITY;
