@@ -306,6 +306,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           kpend[ks] = true;
           kpar[ks] = kph;
           if (++ks == NK_STAGE) { ks = 0; kph ^= 1; }
+          if (i == tl.nblk - 1 && next < p.n_items) {
+            // the next tile's q_nope rows, read with plain loads by the softmax warps when this
+            // tile ends (about two blocks from now), go to L2: two 64-feature boxes of 128 rows.
+            // Earlier, the key/value stream would evict them before use.
+            const Tile nt = tile_of(next, p);
+            tma_prefetch_l2_4d(&tm_q, 0, nt.h, nt.t0, nt.b);
+            tma_prefetch_l2_4d(&tm_q, 64, nt.h, nt.t0, nt.b);
+          }
         }
       }
       if (!ok) {
@@ -470,10 +478,18 @@ __global__ void __launch_bounds__(THREADS, 1)
           p.q + ((static_cast<int64_t>(tl.b) * p.T + (row_valid ? t : 0)) * p.H + tl.h) * 192);
       uint32_t qn[16];
       uint32_t q8[8];
+      uint32_t qw[2][8];   // this part's 32 q_nope features: two 32-byte loads
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        if (row_valid) ldg_v8(qrow + part * 4 + 2 * c, qw[c]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (!row_valid) qw[c][e] = 0u;
+      }
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const uint4 v = row_valid ? __ldg(qrow + part * 4 + c) : make_uint4(0, 0, 0, 0);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t w[4] = {qw[c >> 1][(c & 1) * 4], qw[c >> 1][(c & 1) * 4 + 1], qw[c >> 1][(c & 1) * 4 + 2],
+                               qw[c >> 1][(c & 1) * 4 + 3]};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float lo = __uint_as_float(w[e] << 16);
@@ -507,7 +523,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool got = take_item(0, item);
       ok = quad_sync_and(quad_bar, got);
     }
-    if (ok && item >= 0) prepare_queries(tile_of(item, p));
+    uint32_t first_mask = 0u;   // selection word of the first block of the tile about to start
+    if (ok && item >= 0) {
+      const Tile t0l = tile_of(item, p);
+      const int tt = t0l.t0 + r;
+      first_mask = (tt < p.T) ? __ldg(p.sel_bits + (static_cast<int64_t>(t0l.b) * p.T + tt) * p.W + part) : 0u;
+      prepare_queries(t0l);
+    }
     while (ok && item >= 0) {
       const Tile tl = tile_of(item, p);
       const int t = tl.t0 + r;
@@ -517,7 +539,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           p.sel_bits + (static_cast<int64_t>(tl.b) * p.T + (row_valid ? t : 0)) * p.W + part;
       float m_ref = -INFINITY;   // running reference max, log2 domain (identical in the quadrant's warps)
       float l = 0.f;             // running sum of this thread's columns' probabilities
-      uint32_t mask_next = row_valid ? __ldg(bits_row) : 0u;
+      uint32_t mask_next = first_mask;
       for (int i = 0; i < tl.nblk; ++i, ++g) {
         const uint32_t mask = mask_next;
         if (i + 1 < tl.nblk) mask_next = row_valid ? __ldg(bits_row + (i + 1) * 4) : 0u;
@@ -613,7 +635,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         const bool got = take_item(it + 1, next_item);
         ok = quad_sync_and(quad_bar, got);
       }
-      if (ok && next_item >= 0) prepare_queries(tile_of(next_item, p));
+      if (ok && next_item >= 0) {
+        const Tile nt = tile_of(next_item, p);
+        const int nt_t = nt.t0 + r;
+        // the next tile's first selection word, loaded now so its latency passes during the
+        // query preparation and this tile's epilogue
+        first_mask = (nt_t < p.T) ? __ldg(p.sel_bits + (static_cast<int64_t>(nt.b) * p.T + nt_t) * p.W + part) : 0u;
+        prepare_queries(nt);
+      }
 
       // epilogue: out = O / l (bf16), lse = (m + log2 l) ln 2
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_p));
@@ -639,14 +668,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                        (__uint_as_float(lp[2]) + __uint_as_float(lp[3]));   // same order in every part
       const float inv_l = (lt > 0.f) ? 1.0f / lt : 0.f;
       if (row_valid) {
-        uint4* d4 = reinterpret_cast<uint4*>(
-            p.out + ((static_cast<int64_t>(tl.b) * p.T + t) * p.H + tl.h) * 128 + part * PCOLS);
+        // this part's 32 output features = 64 bytes, as two 32-byte stores (each store instruction
+        // of the warp touches one line per row, so fewer, wider stores take fewer L1 passes)
+        uint16_t* orow = p.out + ((static_cast<int64_t>(tl.b) * p.T + t) * p.H + tl.h) * 128 + part * PCOLS;
 #pragma unroll
-        for (int k = 0; k < PCOLS / 8; ++k) {
-          d4[k] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv_l, __uint_as_float(v[8 * k + 1]) * inv_l),
-                             pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv_l, __uint_as_float(v[8 * k + 3]) * inv_l),
-                             pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv_l, __uint_as_float(v[8 * k + 5]) * inv_l),
-                             pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv_l, __uint_as_float(v[8 * k + 7]) * inv_l));
+        for (int k = 0; k < PCOLS / 16; ++k) {
+          uint32_t o8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            o8[e] = pack_bf16x2(__uint_as_float(v[16 * k + 2 * e]) * inv_l, __uint_as_float(v[16 * k + 2 * e + 1]) * inv_l);
+          stg_v8(orow + 16 * k, o8);
         }
         if (part == 0) {
           const float lse = (lt > 0.f) ? (m_ref + log2f(lt)) * 0.6931471805599453f : -INFINITY;
