@@ -1,5 +1,5 @@
-// Stages 2-3: kv_norm fused into the wkv_b up-projection (tcgen05 GEMM: A in TMEM, W in by TMA,
-// outputs out by TMA tensor stores).
+// Stages 2-3: kv_norm fused into the wkv_b up-projection (tcgen05 GEMM: A in TMEM, W in by TMA
+// multicast within a 2-CTA cluster).
 //
 //   y[r, :]  = bf16( gamma * (c_kv[r, :] * (1 / sqrt(mean(c_kv[r, :]^2) + 1e-6))) )
 //              (RMSNorm class, model.py 281-293: x.float(), mean of squares, x * rsqrt(var + eps),
@@ -21,9 +21,9 @@
 // (256 columns, bf16 pairs) as the A operand of every unit of the tile; W streams through a
 // 8-stage TMA ring of 128 x 64 slices (B operand), and each unit is 32 UMMAs M=128 N=128 K=16
 // into one of two TMEM accumulators, so a unit's epilogue overlaps the next unit's MMAs. The
-// epilogue converts the accumulator, writes it 128-byte-swizzled into one of two shared staging
-// buffers and TMA-stores it (kv: two 64-column boxes, klo: one box); rows past T are clipped by
-// the tensor map. The two CTAs of a cluster take adjacent row tiles and walk the same units; each
+// epilogue converts the accumulator and stores each row straight from registers with 32-byte
+// stores (kv: 256 bytes, klo: 128 bytes per row); staging it in shared memory for TMA stores was
+// slower, since shared memory already carries W twice (TMA write, UMMA read). The two CTAs of a cluster take adjacent row tiles and walk the same units; each
 // loads half of every W slice and multicasts it to both, so W leaves L2 once per cluster. A
 // cluster takes a contiguous range of units, row-tile-major, so it normalises few row tiles.
 //
@@ -43,14 +43,11 @@ constexpr int KATOM = 64;                       // bf16 elements per 128-byte sw
 constexpr int NKATOM = KDIM / KATOM;            // 8
 constexpr int B_STAGE_BYTES = BN * 128;         // 16 KB: 128 W rows x 64 latent features
 constexpr int NSTAGE = 8;
-constexpr int OUT_ATOM = BM * 128;              // 16 KB: 128 rows x 128 bytes, 128-byte swizzle
-constexpr int OUT_STAGE_BYTES = 3 * OUT_ATOM;   // kv: two atoms (128 fp16 columns); klo: one atom
-constexpr int NOUT = 2;
 constexpr int THREADS = 192;
 constexpr int CLUSTER = 2;                      // CTAs per cluster sharing every W slice
 constexpr int B_ROWS_PER_CTA = BN / CLUSTER;    // W rows each CTA of a cluster loads per slice
 constexpr uint16_t CLUSTER_MASK = (1u << CLUSTER) - 1;
-constexpr int TILE_BYTES = NSTAGE * B_STAGE_BYTES + NOUT * OUT_STAGE_BYTES;
+constexpr int TILE_BYTES = NSTAGE * B_STAGE_BYTES;
 
 // Barriers after the tiles in the dynamic shared memory (no static shared memory: the dynamic
 // region then starts 1024-byte aligned, as the 128-byte swizzle needs).
@@ -77,6 +74,8 @@ struct Params {
   int units;               // ceil(n_mtiles / CLUSTER) * H * 2: units of a cluster
   const uint16_t* c_kv;    // [B, T, 512] bf16
   const float* gamma;      // [512]
+  uint16_t* kv_out;        // [B, H, T, 256] fp16
+  uint8_t* klo_out;        // [B, H, T, 128] e4m3
 };
 
 // Named barrier of the epilogue warps that also ANDs `pred` over their 128 threads.
@@ -92,15 +91,13 @@ __device__ __forceinline__ bool epi_sync_and(bool pred) {
 }
 
 __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
-    kvnorm_wkvb_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_kv,
-                       const __grid_constant__ CUtensorMap tm_klo, const Params p) {
+    kvnorm_wkvb_kernel(const __grid_constant__ CUtensorMap tm_w, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {
     if (threadIdx.x == 0) set_error(kErrUnsupportedLayout);
     return;
   }
   uint8_t* sB = smem_raw;
-  uint8_t* sOut = smem_raw + NSTAGE * B_STAGE_BYTES;
   Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem_raw + TILE_BYTES);
   uint64_t& a_free = ctl.a_free;
   uint64_t& a_ready = ctl.a_ready;
@@ -145,8 +142,6 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_w);
-    tma_prefetch_desc(&tm_kv);
-    tma_prefetch_desc(&tm_klo);
   }
   tc_fence_before();
   __syncthreads();
@@ -235,8 +230,7 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
     const int q = warp & 3;
     const int r = q * 32 + lane;               // row within the tile == TMEM lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const bool leader = threadIdx.x == 64;     // issues the TMA stores
-    int cur_m = -1, seg = 0, acc = 0, n_out = 0;
+    int cur_m = -1, seg = 0, acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int u = u_begin; u < u_end; ++u) {
@@ -308,53 +302,45 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
-      // staging buffer n_out & 1 is free once the stores of two units ago have read it
-      if (leader) tma_store_wait_read<1>();
       ok = epi_sync_and(got);
       if (!ok) break;
-      uint8_t* so = sOut + (n_out & 1) * OUT_STAGE_BYTES;
-      // kv: 128 fp16 columns = 16 chunks of 16 bytes; chunk c of row r at atom c / 8, position
-      // (c % 8) ^ (r & 7) (the 128-byte swizzle the tensor map expects)
-      uint32_t hw[BN / 2];
+      const int t_row = t0 + r;
+      if (active && t_row < p.T) {
+        const int64_t prow = (static_cast<int64_t>(b) * p.H + h) * p.T + t_row;
+        uint32_t hw[BN / 2];
 #pragma unroll
-      for (int i = 0; i < BN / 2; ++i) hw[i] = pack_f16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        *reinterpret_cast<uint4*>(so + (c >> 3) * OUT_ATOM + r * 128 + (((c & 7) ^ (r & 7)) * 16)) =
-            make_uint4(hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
-      if (half == 0) {
-        // residual of k_nope after the fp16 rounding, scaled by 2^11, as e4m3: 8 chunks of 16 bytes
+        for (int i = 0; i < BN / 2; ++i) hw[i] = pack_f16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        uint16_t* dst = p.kv_out + prow * 256 + half * BN;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          uint32_t lw[4];
+          uint32_t o8[8];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float rr[4];
+          for (int e = 0; e < 8; ++e) o8[e] = hw[8 * c + e];
+          stg_v8(dst + 16 * c, o8);
+        }
+        if (half == 0) {
+          uint8_t* dlo = p.klo_out + prow * 128;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int k = c * 16 + i * 4 + e;
-              const uint16_t hb = static_cast<uint16_t>((hw[k >> 1] >> ((k & 1) * 16)) & 0xFFFFu);
-              rr[e] = __fmul_rn(__fsub_rn(__uint_as_float(v[k]), f16_bits_to_float(hb)), KLO_SCALE);
+          for (int c = 0; c < 4; ++c) {
+            uint32_t lw[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float rr[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int k = c * 32 + i * 4 + e;
+                const uint16_t hb = static_cast<uint16_t>((hw[k >> 1] >> ((k & 1) * 16)) & 0xFFFFu);
+                rr[e] = __fmul_rn(__fsub_rn(__uint_as_float(v[k]), f16_bits_to_float(hb)), KLO_SCALE);
+              }
+              lw[i] = static_cast<uint32_t>(pack_e4m3x2(rr[0], rr[1])) | (static_cast<uint32_t>(pack_e4m3x2(rr[2], rr[3])) << 16);
             }
-            lw[i] = static_cast<uint32_t>(pack_e4m3x2(rr[0], rr[1])) | (static_cast<uint32_t>(pack_e4m3x2(rr[2], rr[3])) << 16);
+            stg_v8(dlo + 32 * c, lw);
           }
-          *reinterpret_cast<uint4*>(so + 2 * OUT_ATOM + r * 128 + ((c ^ (r & 7)) * 16)) =
-              make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
       }
-      fence_proxy_async_smem();
-      named_sync(EPI_BAR, 128);
-      if (leader && active) {
-        const int plane = b * p.H + h;
-        tma_store_3d(&tm_kv, so, half * BN, t0, plane);
-        tma_store_3d(&tm_kv, so + OUT_ATOM, half * BN + 64, t0, plane);
-        if (half == 0) tma_store_3d(&tm_klo, so + 2 * OUT_ATOM, 0, t0, plane);
-        tma_store_commit();
-      }
-      ++n_out;
     }
     // the stores read shared memory until they complete: wait before the CTA exits
-    if (leader) tma_store_wait_all<0>();
+
   }
 
   tc_fence_before();

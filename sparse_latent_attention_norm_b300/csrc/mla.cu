@@ -100,24 +100,12 @@ mla_status launch_canon(const int32_t* topk_idx, mla_dims d, uint32_t* sel_bits,
 
 mla_status launch_kvnorm_wkvb(const mla_bf16* c_kv, const float* gamma, const mla_bf16* wkv_b, mla_dims d,
                               uint16_t* kv, uint8_t* klo, int num_sms, int k1_max_clusters, cudaStream_t st) {
-  CUtensorMap tm_w, tm_kv, tm_klo;
+  CUtensorMap tm_w;
   {
     const uint64_t dims[2] = {kLatent, static_cast<uint64_t>(d.H) * kKV};
     const uint64_t strides[1] = {kLatent * 2};
     const uint32_t box[2] = {64, mla::k1::B_ROWS_PER_CTA};
     if (!mla::make_tmap_bf16(&tm_w, wkv_b, 2, dims, strides, box)) return MLA_ERR_CUDA;
-  }
-  {  // output kv [B*H planes][T][256] fp16, stored in 64-column x 128-row boxes
-    const uint64_t dims[3] = {kKV, static_cast<uint64_t>(d.T), static_cast<uint64_t>(d.B) * d.H};
-    const uint64_t strides[2] = {kKV * 2, static_cast<uint64_t>(d.T) * kKV * 2};
-    const uint32_t box[3] = {64, mla::k1::BM, 1};
-    if (!mla::make_tmap_f16(&tm_kv, kv, 3, dims, strides, box)) return MLA_ERR_CUDA;
-  }
-  {  // output klo [B*H planes][T][128] bytes, stored in 128-column x 128-row boxes
-    const uint64_t dims[3] = {128, static_cast<uint64_t>(d.T), static_cast<uint64_t>(d.B) * d.H};
-    const uint64_t strides[2] = {128, static_cast<uint64_t>(d.T) * 128};
-    const uint32_t box[3] = {128, mla::k1::BM, 1};
-    if (!mla::make_tmap_u8(&tm_klo, klo, 3, dims, strides, box)) return MLA_ERR_CUDA;
   }
   mla::k1::Params p;
   p.B = d.B;
@@ -131,11 +119,13 @@ mla_status launch_kvnorm_wkvb(const mla_bf16* c_kv, const float* gamma, const ml
   p.units = static_cast<int>(units);
   p.c_kv = c_kv;
   p.gamma = gamma;
+  p.kv_out = kv;
+  p.klo_out = klo;
   // whole clusters, no more than can be resident at once (each cluster's range of units is fixed)
   int clusters = k1_max_clusters > 0 ? k1_max_clusters : num_sms / mla::k1::CLUSTER;
   if (clusters > p.units) clusters = p.units;
   const int grid = clusters * mla::k1::CLUSTER;
-  mla::k1::kvnorm_wkvb_kernel<<<grid, mla::k1::THREADS, mla::k1::SMEM_BYTES, st>>>(tm_w, tm_kv, tm_klo, p);
+  mla::k1::kvnorm_wkvb_kernel<<<grid, mla::k1::THREADS, mla::k1::SMEM_BYTES, st>>>(tm_w, p);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
