@@ -27,6 +27,12 @@ struct DeviceInfo {
   bool ready = false;
   int num_sms = 0;
   int k1_clusters = 0;   // clusters of the GEMM stage that fit on the device at once (0: unknown)
+  // The selection stage runs beside the GEMM stage on this side stream (both only need the
+  // call's inputs; the attention stage needs both): fork and join through two events. Created on
+  // first use; the mutex keeps a call's record / wait pairs together when threads share a device.
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex fork_mutex;
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
@@ -58,11 +64,22 @@ mla_status device_setup(int* num_sms, int* k1_clusters) {
       }
       d.k1_clusters = n;
     }
+    if (cudaStreamCreateWithFlags(&d.side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming) != cudaSuccess)
+      return MLA_ERR_CUDA;
     d.ready = true;
   }
   *num_sms = d.num_sms;
   if (k1_clusters) *k1_clusters = d.k1_clusters;
   return MLA_OK;
+}
+
+// The current device's record (device_setup must have succeeded on it).
+DeviceInfo& current_device_info() {
+  int dev = 0;
+  (void)cudaGetDevice(&dev);
+  return g_dev[dev];
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -297,8 +314,18 @@ mla_status mla_sparse_prefill_ex(const mla_bf16* q, const mla_bf16* c_kv, const 
   uint8_t* klo = base + align_up(kv_bytes(d), 1024);
   uint32_t* bits = reinterpret_cast<uint32_t*>(klo + align_up(klo_bytes(d), 1024));
   uint32_t* sched = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(bits) + align_up(bits_bytes(d), 1024));
-  s = launch_canon(topk_idx, d, bits, n_keys, flags, sched, st);
-  if (s == MLA_OK) s = launch_kvnorm_wkvb(c_kv, gamma, wkv_b, d, kv, klo, sms, k1_clusters, st);
+  {
+    // selection on the side stream, concurrently with the GEMM stage on `st`; the attention stage
+    // on `st` waits for both
+    DeviceInfo& di = current_device_info();
+    std::lock_guard<std::mutex> lock(di.fork_mutex);
+    if (cudaEventRecord(di.fork, st) != cudaSuccess || cudaStreamWaitEvent(di.side, di.fork, 0) != cudaSuccess)
+      s = MLA_ERR_CUDA;
+    if (s == MLA_OK) s = launch_canon(topk_idx, d, bits, n_keys, flags, sched, di.side);
+    if (s == MLA_OK && (cudaEventRecord(di.join, di.side) != cudaSuccess)) s = MLA_ERR_CUDA;
+    if (s == MLA_OK) s = launch_kvnorm_wkvb(c_kv, gamma, wkv_b, d, kv, klo, sms, k1_clusters, st);
+    if (s == MLA_OK && cudaStreamWaitEvent(st, di.join, 0) != cudaSuccess) s = MLA_ERR_CUDA;
+  }
   if (s == MLA_OK) s = launch_sparse_attn(q, k_pe, kv, klo, bits, out, lse, d, sched, sms, st);
   if (owned && cudaFreeAsync(ws, st) != cudaSuccess && s == MLA_OK) s = MLA_ERR_CUDA;
   return s;
