@@ -243,20 +243,22 @@ def run_reference(args, rank, world, dist, budget_s: float = 150.0):
 
 
 def time_stage(fn, flush, stream, warmup, steps):
-    """Mean CUDA-event time (ms) of fn() on `stream`, L2 flushed before every call."""
+    """Mean CUDA-event time (ms) of fn() on `stream`, L2 flushed before every call.
+
+    The calls are enqueued back to back (no host synchronisation between them), as in the timed
+    steps: with a synchronisation after each call the device would idle between the flush and
+    the next launch while the host prepares it, and that gap would land inside the event pair."""
     import torch
-    times = []
-    for i in range(warmup + steps):
+    n = warmup + steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize()
+    for a, b in evs:
         flush.zero_()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
         b.record(stream)
-        b.synchronize()
-        if i >= warmup:
-            times.append(a.elapsed_time(b))
-    return statistics.mean(times)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs[warmup:])
 
 
 def run_ours(args, rank, world, dist):
