@@ -1,5 +1,4 @@
-// Stages 2-3: kv_norm fused into the wkv_b up-projection (tcgen05 GEMM: A in TMEM, W in by TMA
-// multicast within a 2-CTA cluster).
+// Stages 2-3: kv_norm fused into the wkv_b up-projection (tcgen05 GEMM: A in TMEM, W in by TMA).
 //
 //   y[r, :]  = bf16( gamma * (c_kv[r, :] * (1 / sqrt(mean(c_kv[r, :]^2) + 1e-6))) )
 //              (RMSNorm class, model.py 281-293: x.float(), mean of squares, x * rsqrt(var + eps),
@@ -19,13 +18,14 @@
 // unit is one row tile x one half of one head (k_nope: W rows h*256 + [0,128), or v: h*256 +
 // [128,256)) x the whole latent (512). The normalised row tile y (128 x 512 bf16) lives in TMEM
 // (256 columns, bf16 pairs) as the A operand of every unit of the tile; W streams through a
-// 8-stage TMA ring of 128 x 64 slices (B operand), and each unit is 32 UMMAs M=128 N=128 K=16
-// into one of two TMEM accumulators, so a unit's epilogue overlaps the next unit's MMAs. The
-// epilogue converts the accumulator and stores each row straight from registers with 32-byte
-// stores (kv: 256 bytes, klo: 128 bytes per row); staging it in shared memory for TMA stores was
-// slower, since shared memory already carries W twice (TMA write, UMMA read). The two CTAs of a cluster take adjacent row tiles and walk the same units; each
-// loads half of every W slice and multicasts it to both, so W leaves L2 once per cluster. A
-// cluster takes a contiguous range of units, row-tile-major, so it normalises few row tiles.
+// 4-stage TMA ring whose stages hold two 128 x 64 slices (B operand), and each unit is 32 UMMAs
+// M=128 N=128 K=16 into one of two TMEM accumulators, so a unit's epilogue overlaps the next
+// unit's MMAs. The epilogue converts the accumulator and stores each row straight from registers
+// with 32-byte stores (kv: 256 bytes, klo: 128 bytes per row); staging it in shared memory for
+// TMA stores was slower, since shared memory already carries W twice (TMA write, UMMA read). A
+// CTA takes a contiguous range of units, row-tile-major, so it normalises few row tiles. With
+// CLUSTER > 1 the CTAs of a cluster take adjacent row tiles and walk the same units, each
+// loading 1/CLUSTER of every W slice and multicasting it to all, so W leaves L2 once per cluster.
 //
 // Warp roles (192 threads): warp 0 TMA producer of W, warp 1 TMEM owner + MMA issuer, warps 2-5
 // normalise rows into TMEM and run the epilogue (warp w owns TMEM lanes 32*(w%4) .. +31).
@@ -41,13 +41,23 @@ constexpr int BN = 128;                         // outputs per unit (k_nope or v
 constexpr int KDIM = 512;                       // kv_lora_rank
 constexpr int KATOM = 64;                       // bf16 elements per 128-byte swizzle row
 constexpr int NKATOM = KDIM / KATOM;            // 8
-constexpr int B_STAGE_BYTES = BN * 128;         // 16 KB: 128 W rows x 64 latent features
-constexpr int NSTAGE = 8;
+constexpr int ATOM_BYTES = BN * 128;            // 16 KB: 128 W rows x 64 latent features
+// W stages of KPS slices on one barrier: each barrier wait of the MMA thread costs ~170 cycles
+// while its UMMAs are in flight, so a stage carries 8 UMMAs (2 slices), and the TMA engine
+// streams a multi-box stage faster than single boxes.
+constexpr int KPS = 2;                          // latent atoms (64 features) per W stage
+constexpr int STAGES_PER_UNIT = NKATOM / KPS;
+constexpr int B_STAGE_BYTES = KPS * ATOM_BYTES;
+constexpr int NSTAGE = 4;
 constexpr int THREADS = 192;
-constexpr int CLUSTER = 2;                      // CTAs per cluster sharing every W slice
+// CTAs per cluster sharing every W slice by multicast (each loads 1/CLUSTER of a slice's rows).
+// 1: measured faster than 2 once stages carry several slices (multicast halves each CTA's loads
+// but also its TMA rate per byte received).
+constexpr int CLUSTER = 1;
 constexpr int B_ROWS_PER_CTA = BN / CLUSTER;    // W rows each CTA of a cluster loads per slice
 constexpr uint16_t CLUSTER_MASK = (1u << CLUSTER) - 1;
 constexpr int TILE_BYTES = NSTAGE * B_STAGE_BYTES;
+static_assert(NKATOM % KPS == 0, "stages split the latent evenly");
 
 // Barriers after the tiles in the dynamic shared memory (no static shared memory: the dynamic
 // region then starts 1024-byte aligned, as the 128-byte swizzle needs).
@@ -66,6 +76,7 @@ constexpr uint32_t TM_ACC = 256;  // accumulators at columns 256..383 and 384..5
 constexpr float RMS_EPS = 1e-6f;
 constexpr float KLO_SCALE = 2048.0f;   // 2^11
 constexpr int EPI_BAR = 1;             // named barrier of the four epilogue warps
+constexpr int NORM_LOADS = 8;          // 16-byte loads of a c_kv row in flight during the RMSNorm
 
 struct Params {
   int B, T, H;
@@ -162,11 +173,17 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
       bool ok = true;
       for (int u = u_begin; u < u_end && ok; ++u) {
         const int h = (u >> 1) % p.H, half = u & 1;
-        for (int ka = 0; ka < NKATOM; ++ka) {
+        for (int sk = 0; sk < STAGES_PER_UNIT; ++sk) {
           if (!mbar_wait(&b_empty[stage], phase ^ 1, abort_p)) { ok = false; break; }
           mbar_arrive_expect_tx(&b_full[stage], B_STAGE_BYTES);
-          tma_load_2d_multicast(sB + stage * B_STAGE_BYTES + rank * B_ROWS_PER_CTA * 128, &tm_w, &b_full[stage],
-                                ka * KATOM, h * 256 + half * BN + rank * B_ROWS_PER_CTA, CLUSTER_MASK);
+          for (int a = 0; a < KPS; ++a) {
+            uint8_t* dst = sB + stage * B_STAGE_BYTES + a * ATOM_BYTES + rank * B_ROWS_PER_CTA * 128;
+            const int x = (sk * KPS + a) * KATOM, y = h * 256 + half * BN + rank * B_ROWS_PER_CTA;
+            if constexpr (CLUSTER > 1)
+              tma_load_2d_multicast(dst, &tm_w, &b_full[stage], x, y, CLUSTER_MASK);
+            else
+              tma_load_2d(dst, &tm_w, &b_full[stage], x, y);
+          }
           pending[stage] = true;
           pend_parity[stage] = phase;
           if (++stage == NSTAGE) { stage = 0; phase ^= 1; }
@@ -200,16 +217,23 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t d = tmem + TM_ACC + static_cast<uint32_t>(acc * BN);
         bool ok = true;
-        for (int ka = 0; ka < NKATOM; ++ka) {
+        for (int sk = 0; sk < STAGES_PER_UNIT; ++sk) {
           if (!mbar_wait(&b_full[stage], phase, abort_p)) { ok = false; break; }
           tc_fence_after();
           const uint64_t db = d_b0 + static_cast<uint64_t>(stage * (B_STAGE_BYTES >> 4));
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4)
-            umma_ts(d, tmem + TM_A + static_cast<uint32_t>((ka * 4 + k4) * 8), db + k4 * 2, idesc,
-                    (ka | k4) != 0 ? 1u : 0u);
+          for (int a = 0; a < KPS; ++a)
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const int ka = sk * KPS + a;
+              umma_ts(d, tmem + TM_A + static_cast<uint32_t>((ka * 4 + k4) * 8), db + a * (ATOM_BYTES >> 4) + k4 * 2,
+                      idesc, (ka | k4) != 0 ? 1u : 0u);
+            }
           issued = true;
-          umma_commit_multicast(&b_empty[stage], CLUSTER_MASK);
+          if constexpr (CLUSTER > 1)
+            umma_commit_multicast(&b_empty[stage], CLUSTER_MASK);
+          else
+            umma_commit(&b_empty[stage]);
           if (++stage == NSTAGE) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -246,17 +270,24 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
         const int t = t0 + r;
         const bool valid = active && t < p.T;
         const uint4* row = reinterpret_cast<const uint4*>(p.c_kv + (static_cast<int64_t>(b) * p.T + (valid ? t : 0)) * KDIM);
-        float ss = 0.f;   // sum of squares in ascending feature order
-#pragma unroll 4
-        for (int a = 0; a < KDIM / 8; ++a) {
-          const uint4 v = valid ? __ldg(row + a) : make_uint4(0, 0, 0, 0);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        // sum of squares in ascending feature order; the row's 16-byte loads go out 8 at a
+        // time (the tile's rows usually come from DRAM: eight round trips instead of sixteen)
+        float ss = 0.f;
+#pragma unroll 1
+        for (int a0 = 0; a0 < KDIM / 8; a0 += NORM_LOADS) {
+          uint4 vv[NORM_LOADS];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float lo = __uint_as_float(w[e] << 16);
-            const float hi = __uint_as_float(w[e] & 0xFFFF0000u);
-            ss = __fadd_rn(ss, __fmul_rn(lo, lo));
-            ss = __fadd_rn(ss, __fmul_rn(hi, hi));
+          for (int j = 0; j < NORM_LOADS; ++j) vv[j] = valid ? __ldg(row + a0 + j) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int j = 0; j < NORM_LOADS; ++j) {
+            const uint32_t w[4] = {vv[j].x, vv[j].y, vv[j].z, vv[j].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float lo = __uint_as_float(w[e] << 16);
+              const float hi = __uint_as_float(w[e] & 0xFFFF0000u);
+              ss = __fadd_rn(ss, __fmul_rn(lo, lo));
+              ss = __fadd_rn(ss, __fmul_rn(hi, hi));
+            }
           }
         }
         const float var = __fmul_rn(ss, 1.0f / KDIM);   // exact: division by a power of two
