@@ -46,18 +46,26 @@ def measured_peaks():
     return 1800.0, 1400.0, 6400.0, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source with comments and whitespace removed (no source here has `//` or `/*`
+    inside a string literal), so that editing a comment does not count as changing a kernel."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return "".join(text.split())
+
+
 def kernel_sources_sha256() -> str:
-    """sha256 over libmla's kernel sources and header (the inputs of every kernel build)."""
+    """sha256 over the code of libmla's kernel sources and header (the inputs of every kernel
+    build), comments and whitespace excluded."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_latent_attention_norm_b300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
-    with open(os.path.join(ROOT, "include", "mla.h"), "rb") as fh:
-        h.update(fh.read())
+    paths = [os.path.join(csrc, f) for f in sorted(os.listdir(csrc)) if f.endswith((".cu", ".cuh", ".h"))]
+    for path in paths + [os.path.join(ROOT, "include", "mla.h")]:
+        h.update(os.path.basename(path).encode())
+        with open(path, encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()
 
 

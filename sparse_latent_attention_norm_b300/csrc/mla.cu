@@ -26,7 +26,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   bool ready = false;
   int num_sms = 0;
-  int k1_clusters = 0;   // clusters of the GEMM stage that fit on the device at once (0: unknown)
+  int k1_clusters = 0;   // GEMM-stage clusters (of k1::CLUSTER CTAs) resident at once (0: unknown)
   // The selection stage runs beside the GEMM stage on this side stream (both only need the
   // call's inputs; the attention stage needs both): fork and join through two events. Created on
   // first use; the mutex keeps a call's record / wait pairs together when threads share a device.
@@ -51,8 +51,8 @@ mla_status device_setup(int* num_sms, int* k1_clusters) {
                              mla::k2::SMEM_BYTES) != cudaSuccess)
       return MLA_ERR_CUDA;
     {
-      // the GEMM stage's grid is a fixed set of clusters with fixed unit ranges: launch no more
-      // clusters than can be resident together
+      // the GEMM stage's grid is a fixed set of clusters (k1::CLUSTER CTAs each, 1 as built) with
+      // fixed unit ranges: launch no more clusters than can be resident together
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(static_cast<unsigned>(d.num_sms / mla::k1::CLUSTER * mla::k1::CLUSTER));
       cfg.blockDim = dim3(mla::k1::THREADS);

@@ -73,3 +73,13 @@ def test_profiled_traffic_tracks_kernel_sources(tmp_path, monkeypatch):
     (prof / "kernels_headline_full.md").write_text(
         "traffic: kernel=sparse_attn_kernel dram_bytes_per_launch=123 sources_sha256=%s\n" % ("0" * 64))
     assert bench.profiled_traffic("headline") == 123
+
+
+def test_source_hash_ignores_comments_not_code():
+    # the capture's hash follows the kernels' code: a comment or whitespace edit keeps it, a code
+    # edit changes it
+    a = bench._code_only("int x = 1; // one\n/* block\n comment */  float y;\n")
+    b = bench._code_only("int x = 1;   // the value one\nfloat   y; /* other */\n")
+    c = bench._code_only("int x = 2; // one\nfloat y;\n")
+    assert a == b == "intx=1;floaty;"
+    assert c != a
