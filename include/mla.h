@@ -156,6 +156,18 @@ MLA_API mla_status mla_clear_status(void);
 /* The softmax scale the kernels use: 192^-0.5 * (1 + 0.1 ln 40)^2. Host-only. */
 MLA_API double mla_softmax_scale(void);
 
+/* Diagnostic of the device-side failure path; no part of the prefill. Enqueues on `stream` one
+ * thread that waits, through the same bounded wait every kernel uses, on a barrier nothing
+ * arrives on. After the wait limit (about 2 s) the wait gives up, MLA_ERR_TIMEOUT is recorded in
+ * the status word and the kernel returns; the context stays usable. Read the status with
+ * mla_get_status() and reset it with mla_clear_status() before further work: while the timeout
+ * is recorded, waits in later kernels give up early (they take it for another CTA's timeout).
+ *   result  [2] int32 device memory, 4-byte aligned (written): [0] = 1 if the wait completed
+ *           (it must not), [1] = milliseconds waited.
+ * Returns MLA_OK once the kernel is enqueued, MLA_ERR_INVALID_ARG for a null or misaligned
+ * `result`. */
+MLA_API mla_status mla_selftest_wait_timeout(int32_t* result, void* stream);
+
 /* A static, human-readable name for a status code. Host-only. */
 MLA_API const char* mla_status_string(mla_status s);
 

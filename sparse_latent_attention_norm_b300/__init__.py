@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
 # every entry point include/mla.h declares
 SYMBOLS = ("mla_sparse_prefill_workspace_size", "mla_sparse_prefill", "mla_sparse_prefill_ex", "mla_canon_select",
            "mla_kvnorm_wkvb", "mla_sparse_attention", "mla_get_status", "mla_clear_status", "mla_softmax_scale",
-           "mla_status_string", "mla_sparse_prefill_noalloc")
+           "mla_status_string", "mla_sparse_prefill_noalloc", "mla_selftest_wait_timeout")
 
 
 class MlaError(RuntimeError):
@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
         L.mla_status_string.argtypes = [I]
         L.mla_sparse_prefill_noalloc.restype = I
         L.mla_sparse_prefill_noalloc.argtypes = [P] * 8 + [Dims, P]
+        L.mla_selftest_wait_timeout.restype = I
+        L.mla_selftest_wait_timeout.argtypes = [P, P]
         _lib = L
     return _lib
 
@@ -125,6 +127,19 @@ def get_status() -> int:
 
 def clear_status() -> None:
     _check(lib().mla_clear_status(), "mla_clear_status")
+
+
+def selftest_wait_timeout(stream=None) -> tuple[int, int]:
+    """Run mla_selftest_wait_timeout and wait for it: (1 if the wait completed else 0, milliseconds
+    waited). It leaves MLA_ERR_TIMEOUT in the status word; clear_status() resets it."""
+    import torch
+    res = torch.zeros(2, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream() if stream is None else stream
+    _check(lib().mla_selftest_wait_timeout(ctypes.c_void_p(res.data_ptr()), ctypes.c_void_p(s.cuda_stream)),
+           "mla_selftest_wait_timeout")
+    s.synchronize()
+    completed, ms = (int(x) for x in res.cpu().tolist())
+    return completed, ms
 
 
 def alloc_workspace(B: int, T: int, H: int, K: int, device=None):

@@ -15,6 +15,25 @@
 #include "kvnorm_wkvb.cuh"
 #include "sparse_attn.cuh"
 
+namespace mla {
+
+// Diagnostic of the failure path: one thread waits, through the bounded wait every kernel uses,
+// on an mbarrier nothing arrives on. The wait gives up at its limit, records the timeout in the
+// status word and returns. result[0] = 1 if the wait completed, result[1] = milliseconds waited.
+__global__ void selftest_wait_timeout_kernel(int32_t* result) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    const uint64_t t0 = globaltimer_ns();
+    const bool completed = mbar_wait(&bar, 0, nullptr);
+    result[0] = completed ? 1 : 0;
+    result[1] = static_cast<int32_t>((globaltimer_ns() - t0) / 1000000ull);
+  }
+}
+
+}  // namespace mla
+
 namespace {
 
 constexpr int kLatent = 512, kQK = 192, kRope = 64, kKV = 256;
@@ -408,6 +427,12 @@ mla_status mla_get_status(void) {
   for (int code = 1; code < 32; ++code)
     if (word & (1u << code)) return static_cast<mla_status>(code);
   return MLA_OK;
+}
+
+mla_status mla_selftest_wait_timeout(int32_t* result, void* stream) {
+  if (result == nullptr || (reinterpret_cast<uintptr_t>(result) & 3u) != 0) return MLA_ERR_INVALID_ARG;
+  mla::selftest_wait_timeout_kernel<<<1, 32, 0, as_stream(stream)>>>(result);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 mla_status mla_clear_status(void) {
