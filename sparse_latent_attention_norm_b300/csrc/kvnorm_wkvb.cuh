@@ -163,8 +163,8 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer: this CTA's part of every W slice
-    // A slice stage is refilled once every CTA of the cluster has consumed it (b_empty counts
-    // one commit per CTA); the own b_full expects the whole slice, whose parts arrive from all.
+    // A stage is refilled once every CTA of the cluster has consumed it (b_empty counts one commit
+    // per CTA); the own b_full expects the whole stage, whose parts arrive from every CTA.
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -199,7 +199,7 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(BM, BN, false, false);
-      const uint64_t d_b0 = sdesc_sw128(smem_u32(sB), 16, 1024);   // + stage * (16 KB >> 4) + k4 * 2
+      const uint64_t d_b0 = sdesc_sw128(smem_u32(sB), 16, 1024);   // + stage and slice offsets >> 4, + k4 * 2
       int cur_m = -1, seg = 0, stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool issued = false;
