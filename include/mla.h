@@ -74,7 +74,8 @@ typedef struct {
  * each 1024-byte aligned. Calls that run at the same time need workspaces of their own. */
 MLA_API size_t mla_sparse_prefill_workspace_size(mla_dims d);
 
-/* The whole prefill path: kv_norm -> wkv_b -> sparse causal attention.
+/* The whole prefill path: kv_norm -> wkv_b -> sparse causal attention (steps 1-4 above: "Key-value
+ * RMSNorm", "Keys", "Split value heads" and "Scale scores" pages; MHA prefill, model.py 574-589).
  *   q         [B, T, H, 192] bf16: features 0..127 pair with k_nope, 128..191 (rotary, already
  *             applied) with k_pe. Features 0..127 are used in fp16 (exact for magnitudes in
  *             [2^-14, 65504]; smaller ones lose low bits, larger ones overflow).
@@ -102,15 +103,18 @@ MLA_API mla_status mla_sparse_prefill_ex(const mla_bf16* q, const mla_bf16* c_kv
                                  mla_dims d, void* workspace, size_t workspace_bytes, void* stream,
                                  int32_t* n_keys, unsigned flags);
 
-/* Stage 1 alone (the index mask of the MHA prefill excerpt, without materialising it):
- * canonical selection bitsets. Bit (j % 32) of word sel_bits[(b*T + t)*W + j/32], W =
+/* Stage 1 alone: the index mask of the MHA prefill excerpt ("Keys" page, model.py 574-589: -inf
+ * scattered to 0 at the top-k indices, plus the causal mask), written as canonical selection
+ * bitsets instead of a [B, T, T] mask. Bit (j % 32) of word sel_bits[(b*T + t)*W + j/32], W =
  * ceil(T/128)*4, is set iff key j is selected for query t (0 <= j <= t). Words of row t at or
  * beyond (t/128 + 1)*4 are not written. n_keys [B, T] int32 may be NULL. */
 MLA_API mla_status mla_canon_select(const int32_t* topk_idx, mla_dims d, uint32_t* sel_bits, int32_t* n_keys,
                             unsigned flags, void* stream);
 
-/* Stages 2-3 alone: kv_norm fused into the wkv_b GEMM. For head h at position t, with k_nope and v
- * the up-projected features (fp32 accumulation of bf16 products):
+/* Stages 2-3 alone: kv_norm (RMSNorm class, model.py 281-293, "Key-value RMSNorm" page) fused into
+ * the wkv_b GEMM (ColumnParallelLinear, MLA __init__ and MHA prefill on the "Keys" and "Split value
+ * heads" pages). For head h at position t, with k_nope and v the up-projected features (fp32
+ * accumulation of bf16 products):
  *   kv  [B, H, T, 256] fp16 (IEEE binary16 bit patterns): kv[.., 0:128] = k_hi = fp16(k_nope),
  *       kv[.., 128:256] = fp16(v);
  *   klo [B, H, T, 128] fp8 e4m3 bytes: (k_nope - k_hi) * 2^11, the part of k_nope fp16 drops.
@@ -118,9 +122,10 @@ MLA_API mla_status mla_canon_select(const int32_t* topk_idx, mla_dims d, uint32_
 MLA_API mla_status mla_kvnorm_wkvb(const mla_bf16* c_kv, const float* gamma, const mla_bf16* wkv_b, mla_dims d,
                            uint16_t* kv, uint8_t* klo, void* stream);
 
-/* Stage 4 alone: sparse causal attention from the outputs of the two stages above. Its tile
- * counter is one library-owned word per device, zeroed on `stream` before the launch: calls of
- * this entry point that can overlap on one device (other streams, other threads) race on it. */
+/* Stage 4 alone: sparse causal attention ("Keys" and "Scale scores" pages; MHA prefill, model.py
+ * 574-589) from the outputs of the two stages above. Its tile counter is one library-owned word
+ * per device, zeroed on `stream` before the launch: calls of this entry point that can overlap on
+ * one device (other streams, other threads) race on it. */
 MLA_API mla_status mla_sparse_attention(const mla_bf16* q, const mla_bf16* k_pe, const uint16_t* kv,
                                 const uint8_t* klo, const uint32_t* sel_bits, mla_bf16* out, float* lse,
                                 mla_dims d, void* stream);
