@@ -96,6 +96,8 @@ def test_argument_errors_return_before_any_device_work(L):
     assert L.mla_kvnorm_wkvb(P(good[0]), P(good[1]), P(good[2]), d, P(good[3]), None, None) == 1
     assert L.mla_sparse_attention(P(good[0]), P(good[1]), P(good[2]), P(good[3]), P(good[4]), P(good[5]), None, d,
                                   None) == 1
+    assert L.mla_selftest_wait_timeout(None, None) == 1             # null result
+    assert L.mla_selftest_wait_timeout(P(good[0] + 2), None) == 1    # misaligned result
 
 
 def test_binding_fails_loudly_without_cuda_tensors():
