@@ -22,7 +22,7 @@
 // M=128 N=128 K=16 into one of two TMEM accumulators, so a unit's epilogue overlaps the next
 // unit's MMAs. The epilogue converts the accumulator and stores each row straight from registers
 // with 32-byte stores (kv: 256 bytes, klo: 128 bytes per row); staging it in shared memory for
-// TMA stores was slower, since shared memory already carries W twice (TMA write, UMMA read). A
+// TMA stores measured slower. A
 // CTA takes a contiguous range of units, row-tile-major, so it normalises few row tiles. With
 // CLUSTER > 1 the CTAs of a cluster take adjacent row tiles and walk the same units, each
 // loading 1/CLUSTER of every W slice and multicasting it to all, so W leaves L2 once per cluster.
