@@ -7,6 +7,12 @@ over one batch of seeded synthetic inputs resident in HBM, with a preallocated w
 timed step is bracketed by CUDA events on the launching stream; a 256 MB buffer write between
 steps (outside the event pair) flushes the 126 MB L2. Rank 0 prints one JSON line.
 
+Besides the headline workload the line carries a sustained figure (the same step back to back
+for a few seconds, against the measured sustained peak) and `per_config`: every other workload
+(tiny, dense_causal, stress, long_context) timed the same way, each with its formula TFLOP/s,
+queries*heads/s, fractions of peak, the attention stage alone, the hardware/formula MMA ratio and
+the oracle on a bounded sample (single-threaded too on tiny and dense_causal).
+
 Metric: formula TFLOP/s = (2*B*T*H*512*256 + 2*H*sum_n*(192+128)) / time, sum_n being the number of
 distinct causal selected keys summed over all queries (counted by the library's n_keys output).
 
@@ -36,6 +42,20 @@ def formula_flops(B, T, H, sum_n):
     up = 2.0 * B * T * H * 512 * 256
     attn = 2.0 * H * sum_n * (192 + 128)
     return up, attn
+
+
+def hardware_mma_flops(B, T, H):
+    """(GEMM stage, attention stage) tensor-core work the kernels issue, in 16-bit-equivalent flops
+    (an f8f6f4 UMMA of K=32 takes the time of a 16-bit one of K=16 and is counted as that):
+      GEMM stage: per 128-row tile, head and half (k_nope or v), 32 UMMAs of 128x128x16;
+      attention: per (batch, head, 128-query tile qt) qt + 1 key blocks of 24 UMMAs of 128x128x16
+      (8 fp16 q_nope.k_hi, 4 bf16 q_pe.k_pe, 4 f8 residual, 8 fp16 P.V), over the whole block
+      whether or not a key is selected."""
+    umma = 2.0 * 128 * 128 * 16
+    nqt = (T + 127) // 128
+    gemm = B * nqt * H * 2 * 32 * umma
+    attn = B * H * (nqt * (nqt + 1) // 2) * 24 * umma
+    return gemm, attn
 
 
 def measured_peaks():
@@ -183,13 +203,13 @@ class ClockSampler:
             return self.parse(f)
 
 
-def cpu_baseline(inp, w, seconds_hint: float = 15.0):
+def cpu_baseline(inp, w, seconds_hint: float = 15.0, threads: int = 0):
     """The fp64 oracle, as it stands, on a bounded sample: all query rows of the first heads (at
-    least one head per core: the oracle runs one thread per (batch, head)), doubling the head
-    count until one run takes about `seconds_hint` / 2 or more."""
+    least one head per thread: the oracle runs one thread per (batch, head)), doubling the head
+    count until one run takes about `seconds_hint` / 2 or more. threads = 0: all host cores."""
     import numpy as np
     import oracle
-    cores = os.cpu_count() or 1
+    cores = threads if threads > 0 else (os.cpu_count() or 1)
     heads, dt, nk = min(w.H, cores), 0.0, None
     while True:
         t0 = time.perf_counter()
@@ -201,8 +221,9 @@ def cpu_baseline(inp, w, seconds_hint: float = 15.0):
     sum_n = float(np.asarray(nk, dtype=np.int64).sum())
     up, attn = formula_flops(w.B, w.T, heads, sum_n)
     return {"value": (up + attn) / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "queries_heads_per_s": w.B * w.T * heads / dt,
             "sample": f"{w.name}: heads 0..{heads - 1} of {w.H}, all {w.B * w.T} query rows, fp64 oracle, "
-                      f"{dt:.1f} s"}
+                      f"{dt:.1f} s on {cores} thread(s)"}
 
 
 def run_reference(args, rank, world, dist, budget_s: float = 150.0):
@@ -269,6 +290,136 @@ def time_stage(fn, flush, stream, warmup, steps):
     return statistics.mean(a.elapsed_time(b) for a, b in evs[warmup:])
 
 
+def make_device_inputs(w, dev, batch=None):
+    """Seeded host inputs of workload `w` (optionally with its batch cut to `batch`) and their
+    device copies."""
+    import torch
+    import mla_inputs as mi
+    if batch is not None and batch != w.B:
+        w = mi.custom(w.name + f"_b{batch}", batch, w.T, w.H, w.K, w.pattern, stress=w.stress, seed_id=w.seed_id,
+                      recent=w.recent)
+    host = mi.make_inputs(w)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    return w, host, d
+
+
+def time_steps(step, flush, stream, warmup, steps):
+    """Per-step CUDA-event times (ms) of `steps` calls of step() after `warmup` untimed ones, the
+    L2 flushed (256 MB write) before each call outside its event pair."""
+    import torch
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+
+def measure_config(w, host, d, dev, flush, stream, warmup, steps, peak_burst, cpu_seconds, single_thread):
+    """Formula TFLOP/s, queries*heads/s, fractions of peak, the attention stage alone and the
+    hardware/formula MMA ratio of one workload, next to the oracle on a bounded sample."""
+    import torch
+    import sparse_latent_attention_norm_b300 as mla
+    B, T, H, K = w.B, w.T, w.H, w.K
+    ws = mla.alloc_workspace(B, T, H, K, device=dev)
+    out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, T, H), dtype=torch.float32, device=dev)
+    _, _, nk = mla.sparse_prefill(d["q"], d["c_kv"], d["k_pe"], d["gamma"], d["wkv_b"], d["topk_idx"],
+                                  workspace=ws, n_keys=True)
+    sum_n = float(nk.to(torch.int64).sum().item())
+    up, attn = formula_flops(B, T, H, sum_n)
+    hw_gemm, hw_attn = hardware_mma_flops(B, T, H)
+
+    def step():
+        mla.sparse_prefill(d["q"], d["c_kv"], d["k_pe"], d["gamma"], d["wkv_b"], d["topk_idx"], out=out, lse=lse,
+                           workspace=ws, stream=stream)
+
+    ms = statistics.mean(time_steps(step, flush, stream, warmup, steps))
+    bits, _ = mla.canon_select(d["topk_idx"], T, n_keys=False)
+    kv, klo = mla.kvnorm_wkvb(d["c_kv"], d["gamma"], d["wkv_b"])
+    attn_ms = time_stage(lambda: mla.sparse_attention(d["q"], d["k_pe"], kv, klo, bits, stream=stream),
+                         flush, stream, warmup, steps)
+    status = mla.get_status()
+    if status != 0:
+        raise SystemExit(f"device status {mla.status_string(status)} after timing {w.name}")
+    del kv, klo, bits, ws, out, lse
+    res = {
+        "B": B, "T": T, "H": H, "K": K, "sum_selected_keys": int(sum_n), "steps": steps,
+        "ms_per_step": ms,
+        "formula_tflops": (up + attn) / (ms / 1e3) / 1e12,
+        "queries_heads_per_s": B * T * H / (ms / 1e3),
+        "frac_of_measured_bf16": (up + attn) / (ms / 1e3) / 1e12 / peak_burst,
+        "frac_of_spec_bf16": (up + attn) / (ms / 1e3) / 1e12 / SPEC_BF16_TFLOPS,
+        "attn_ms": attn_ms,
+        "attn_formula_tflops": attn / (attn_ms / 1e3) / 1e12,
+        "attn_frac_of_measured_bf16": attn / (attn_ms / 1e3) / 1e12 / peak_burst,
+        "hw_to_formula_mma": (hw_gemm + hw_attn) / (up + attn),
+        "attn_hw_to_formula_mma": hw_attn / attn,
+        "attn_hw_tflops": hw_attn / (attn_ms / 1e3) / 1e12,
+        "cpu_baseline": cpu_baseline(host, w, seconds_hint=cpu_seconds),
+    }
+    if single_thread:
+        res["cpu_baseline_1_thread"] = cpu_baseline(host, w, seconds_hint=cpu_seconds, threads=1)
+    return res
+
+
+def fp8_weight_of(wkv_b):
+    """An FP8 block-scaled copy of a bf16 wkv_b for the benchmark's variant: per 128 x 128 block,
+    scale = max|w| / 448 and e4m3 codes of w / scale (torch's float8 cast, outside any timed
+    region; the scale rule is the one the library reads for the latent)."""
+    import torch
+    rows = wkv_b.shape[0]
+    blocks = wkv_b.float().reshape(rows // 128, 128, 4, 128)
+    amax = blocks.abs().amax(dim=(1, 3))
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    q = (blocks / scale[:, None, :, None]).to(torch.float8_e4m3fn)
+    return q.reshape(rows, 512).view(torch.uint8).contiguous(), scale.contiguous()
+
+
+def measure_variants(w, d, dev, flush, stream, steps, total_flops):
+    """Headline step time with each option of mla_sparse_prefill_opt on, and all of them."""
+    import torch
+    import sparse_latent_attention_norm_b300 as mla
+    B, T, H, K = w.B, w.T, w.H, w.K
+    w8, scale = fp8_weight_of(d["wkv_b"])
+    kv_cache = torch.empty((B, T, 512), dtype=torch.bfloat16, device=dev)
+    pe_cache = torch.empty((B, T, 64), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, T, H), dtype=torch.float32, device=dev)
+    cases = {
+        "fp8_wkv_b": dict(wkv_b=w8, wkv_b_scale=scale),
+        "fp8_latent_and_kv_cache": dict(fp8_latent=True, kv_cache=kv_cache, pe_cache=pe_cache),
+        "yarn_rope": dict(rope=True),
+        "all": dict(wkv_b=w8, wkv_b_scale=scale, fp8_latent=True, rope=True, kv_cache=kv_cache, pe_cache=pe_cache),
+    }
+    res = {}
+    for name, kw in cases.items():
+        kw = dict(kw)
+        wkv = kw.pop("wkv_b", d["wkv_b"])
+        opt = mla.options(flags=(mla.FLAG_ROPE if kw.get("rope") else 0),
+                          wkv_b_scale=kw.get("wkv_b_scale"))
+        ws = mla.alloc_workspace(B, T, H, K, device=dev, opt=opt)
+
+        def step():
+            mla.sparse_prefill(d["q"], d["c_kv"], d["k_pe"], d["gamma"], wkv, d["topk_idx"], out=out, lse=lse,
+                               workspace=ws, stream=stream, **kw)
+
+        ms = statistics.mean(time_steps(step, flush, stream, 3, steps))
+        res[name] = {"ms_per_step": ms, "formula_tflops": total_flops / (ms / 1e3) / 1e12, "steps": steps}
+        del ws
+    status = mla.get_status()
+    if status != 0:
+        raise SystemExit(f"device status {mla.status_string(status)} after the variants")
+    return res
+
+
 def run_ours(args, rank, world, dist):
     import torch
 
@@ -280,9 +431,7 @@ def run_ours(args, rank, world, dist):
         raise SystemExit("bench.py needs a CUDA device")
     mla_build.build()
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = mi.WORKLOADS[args.workload]
-    host = mi.make_inputs(w)
-    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    w, host, d = make_device_inputs(mi.WORKLOADS[args.workload], dev, args.batch)
     B, T, H, K = w.B, w.T, w.H, w.K
     ws = mla.alloc_workspace(B, T, H, K, device=dev)
     out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=dev)
@@ -300,6 +449,7 @@ def run_ours(args, rank, world, dist):
     sum_n = float(nk.to(torch.int64).sum().item())
     up_flops, attn_flops = formula_flops(B, T, H, sum_n)
     total_flops = up_flops + attn_flops
+    hw_gemm, hw_attn = hardware_mma_flops(B, T, H)
     mla.clear_status()
 
     for _ in range(args.warmup):
@@ -342,6 +492,16 @@ def run_ours(args, rank, world, dist):
                            flush, stream, args.warmup, n_stage)
     del kv, klo, bits
 
+    # sustained: the same step back to back for about `sustain_s` seconds (the part settles at its
+    # power cap), against the measured sustained bf16 peak
+    sustained = None
+    if args.sustain_s > 0:
+        n_sus = max(args.steps, int(args.sustain_s * 1e3 / max(ms, 1e-3)))
+        with ClockSampler(torch.cuda.current_device()) as sus_clocks:
+            sus_ms = statistics.mean(time_steps(step, flush, stream, 0, n_sus))
+        sustained = {"steps": n_sus, "ms_per_step": sus_ms, "value": world * total_flops / (sus_ms / 1e3) / 1e12,
+                     "unit": "TFLOP/s", "clocks": sus_clocks.summary()}
+
     # end to end from pinned host memory through the public API: every step copies its inputs
     # host->device and its results device->host; the pipeline overlaps step i's input copies with
     # step i-1's compute and step i-2's result copies (copy engines in both directions)
@@ -358,10 +518,35 @@ def run_ours(args, rank, world, dist):
         pipe.result(hnd)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, dist)
+    del pipe, hin
 
     if rank != 0:
         return
     peak_burst, peak_sust, hbm, peak_kind = measured_peaks()
+    if sustained is not None:
+        sustained.update(peak=peak_sust, frac=sustained["value"] / world / peak_sust,
+                         peak_kind=f"{peak_kind} bf16 sustained")
+    cpu = cpu_baseline(host, w)
+
+    # the headline step with the model's own steps around the MHA excerpt switched on (FP8
+    # block-scaled wkv_b, FP8 round trip of the latent with the KV-cache write, YaRN RoPE of q and
+    # k_pe), each timed like the main step
+    variants = {}
+    if not args.no_per_config:
+        variants = measure_variants(w, d, dev, flush, stream, args.config_steps, total_flops)
+
+    # every other workload of the metric's family, one after the other on this GPU
+    per_config = {}
+    if not args.no_per_config:
+        del ws, out, lse, d
+        torch.cuda.empty_cache()
+        for name in [n for n in mi.WORKLOADS if n != w.name]:
+            wc, hc, dc = make_device_inputs(mi.WORKLOADS[name], dev)
+            per_config[name] = measure_config(wc, hc, dc, dev, flush, stream, 3, args.config_steps, peak_burst,
+                                              cpu_seconds=6.0, single_thread=name in ("tiny", "dense_causal"))
+            del hc, dc
+            torch.cuda.empty_cache()
+
     achieved = attn_flops / (attn_avg / 1e3) / 1e12
     value = world * total_flops / (ms / 1e3) / 1e12
     line = {
@@ -385,16 +570,24 @@ def run_ours(args, rank, world, dist):
         "queries_heads_per_s": world * B * T * H / (ms / 1e3),
         "kernel_ms": {"sparse_attn": attn_avg, "kvnorm_wkvb": gemm_avg, "canon_select": canon_avg},
         "kvnorm_wkvb_tflops": up_flops / (gemm_avg / 1e3) / 1e12,
+        "hw_to_formula_mma": (hw_gemm + hw_attn) / total_flops,
+        "attn_hw_to_formula_mma": hw_attn / attn_flops,
+        "attn_hw_tflops": hw_attn / (attn_avg / 1e3) / 1e12,
         "roofline": {"kernel": "sparse_attn_kernel", "bound": "tensor", "achieved": achieved, "peak": peak_burst,
                      "unit": "TFLOP/s", "frac": achieved / peak_burst, "traffic": profiled_traffic(w.name),
                      "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                      "peak_kind": f"{peak_kind} bf16 burst",
                      "algorithmic": "2*H*sum_n*(192+128) flops per launch"},
-        "cpu_baseline": cpu_baseline(host, w),
+        "sustained": sustained,
+        "cpu_baseline": cpu,
         "e2e": {"value": world * total_flops / e2e_s / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": pipe.h2d_bytes(hin), "d2h_bytes_per_step": pipe.d2h_bytes(),
+                "h2d_bytes_per_step": sum(host[k].numel() * host[k].element_size()
+                                          for k in ("q", "c_kv", "k_pe", "gamma", "wkv_b", "topk_idx")),
+                "d2h_bytes_per_step": B * T * H * 128 * 2 + B * T * H * 4,
                 "how": "HostPrefillPipeline: pinned host inputs -> device -> pinned host results each step, "
                        "steps overlapped on three streams"},
+        "variants": variants,
+        "per_config": per_config,
         "gpu_launches": 3 * args.steps,
         "clocks": clocks.summary(),
     }
@@ -410,6 +603,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--kernels-only", action="store_true",
                     help="time the prefill steps only (no stage timings, e2e or CPU baseline): for profilers")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="cut the workload's batch to this many sequences (smaller profiler captures)")
+    ap.add_argument("--sustain-s", type=float, default=4.0,
+                    help="seconds of back-to-back steps for the sustained figure (0: skip)")
+    ap.add_argument("--config-steps", type=int, default=10, help="timed steps per other workload")
+    ap.add_argument("--no-per-config", action="store_true", help="time the chosen workload only")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, dist = dist_setup()

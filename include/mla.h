@@ -15,12 +15,14 @@
  *
  * Conventions shared by every entry point:
  *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous row-major, 16-byte
- *     aligned. bf16 tensors are passed as mla_bf16 (the raw 16-bit pattern).
+ *     aligned (q and out: 32-byte aligned; lse: 4-byte). bf16 tensors are passed as mla_bf16 (the
+ *     raw 16-bit pattern).
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default stream). No call
  *     synchronizes the device unless its comment says so.
  *   - Argument and shape errors are returned synchronously and nothing is enqueued.
  *   - Errors found on the device (a barrier wait that ran out, an index outside [0, T) when
- *     MLA_FLAG_VALIDATE_INDICES is set) are OR-ed into a per-device status word that
+ *     MLA_FLAG_VALIDATE_INDICES is set, a value outside the range the kernels carry exactly, a
+ *     failed bounds check of the checked build) are OR-ed into a per-device status word that
  *     mla_get_status() reads after the caller synchronizes.
  *   - Index convention: key j is used by query t iff j occurs in topk_idx[b, t, :] and 0 <= j <= t.
  *     Duplicates count once; order does not matter; j < 0 or j > t (including j >= T) is ignored.
@@ -52,7 +54,12 @@ typedef enum {
   MLA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
   MLA_ERR_INDEX = 4,       /* device: an index outside [0, T) under MLA_FLAG_VALIDATE_INDICES */
   MLA_ERR_TIMEOUT = 5,     /* device: a barrier wait ran past its limit; the kernel unwound */
-  MLA_ERR_WORKSPACE = 6    /* workspace pointer misaligned or smaller than required */
+  MLA_ERR_WORKSPACE = 6,   /* workspace pointer misaligned or smaller than required */
+  MLA_ERR_RANGE = 7,       /* device: a value left the range the kernels carry exactly: |q[..., 0:128]|
+                            * above 65504 (fp16), |k_nope| at or above 512 (its e4m3 residual would
+                            * saturate) or |v| above 65504 (fp16), NaN included; results are unusable */
+  MLA_ERR_BOUNDS = 8       /* device, checked build only (compiled with MLA_CHECKS): an index or TMA
+                            * coordinate fell outside its tensor; the access was skipped */
 } mla_status;
 
 /* Problem sizes. The feature widths are fixed by the model: latent 512, 128 non-rotary + 64
@@ -66,6 +73,9 @@ typedef struct {
 } mla_dims;
 
 #define MLA_FLAG_VALIDATE_INDICES 1u /* report indices outside [0, T) as MLA_ERR_INDEX */
+#define MLA_FLAG_FP8_LATENT 2u       /* FP8 round trip of the normalised latent before wkv_b (see
+                                      * mla_prefill_options) */
+#define MLA_FLAG_ROPE 4u             /* q[..., 128:192] and k_pe are unrotated: apply YaRN RoPE */
 
 /* Bytes of device workspace mla_sparse_prefill needs for `d` (0 if `d` is invalid): the
  * up-projected keys/values kv [B, H, T, 256] fp16, the key residuals klo [B, H, T, 128] (1 byte
@@ -95,6 +105,15 @@ MLA_API mla_status mla_sparse_prefill(const mla_bf16* q, const mla_bf16* c_kv, c
                               const mla_bf16* wkv_b, const int32_t* topk_idx, mla_bf16* out, float* lse,
                               mla_dims d, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Range of the values the kernels carry exactly (see MLA_ERR_RANGE), checked on every call:
+ *   q[..., 0:128] is used in fp16: |q| <= 65504 (bf16 values of magnitude below 2^-14 lose low
+ *     bits, an absolute error below 2^-25 per feature);
+ *   k_nope is kept as fp16 k_hi plus an e4m3 residual (k_nope - k_hi) * 2^11: |k_nope| < 512;
+ *   v is kept in fp16: |v| <= 65504. */
+#define MLA_MAX_ABS_Q_NOPE 65504.0f
+#define MLA_MAX_ABS_K_NOPE 512.0f
+#define MLA_MAX_ABS_V 65504.0f
+
 /* As mla_sparse_prefill, plus:
  *   n_keys  [B, T] int32 (written unless NULL): size of each query's selected key set.
  *   flags   MLA_FLAG_VALIDATE_INDICES or 0. */
@@ -102,6 +121,54 @@ MLA_API mla_status mla_sparse_prefill_ex(const mla_bf16* q, const mla_bf16* c_kv
                                  const mla_bf16* wkv_b, const int32_t* topk_idx, mla_bf16* out, float* lse,
                                  mla_dims d, void* workspace, size_t workspace_bytes, void* stream,
                                  int32_t* n_keys, unsigned flags);
+
+/* Options of mla_sparse_prefill_opt: the steps of the model's prefill around the MHA excerpt that
+ * the plain entry points leave to the caller. Zero-initialise and set what is wanted.
+ *   flags        MLA_FLAG_VALIDATE_INDICES, and:
+ *     MLA_FLAG_FP8_LATENT  the KV cache's FP8 round trip of the normalised latent before wkv_b
+ *                  ("Keys" page, KV-cache excerpt, model.py 541-573: act_quant(kv, 128), then
+ *                  fp8 * scale cast back to bf16). Per block of 128 latent features: scale =
+ *                  max|y| / 448 (1 for an all-zero block), e4m3 = nearest(y / scale) in fp32,
+ *                  y' = bf16(e4m3 * scale) (act_quant's format and scale rule are not on the
+ *                  pages; this is the plain reading).
+ *     MLA_FLAG_ROPE        q[..., 128:192] and k_pe arrive unrotated; YaRN RoPE is applied at
+ *                  positions 0..T-1 ("Key-value down-projection" page, model.py 565-568;
+ *                  ModelArgs: rope_theta 10000, rope_factor 40, beta_fast 32, beta_slow 1,
+ *                  original_seq_len 4096). Pairs (2i, 2i+1) rotate by t * f_i, f_i YaRN's
+ *                  frequencies; the rotation is done in fp32 from the fp64 angle and rounded to
+ *                  bf16.
+ *   n_keys       [B, T] int32 written unless NULL (as mla_sparse_prefill_ex).
+ *   wkv_b_scale  NULL: wkv_b is bf16 [H*256, 512]. Otherwise wkv_b holds FP8 e4m3 bytes
+ *                [H*256, 512] and this is fp32 [2H, 4], one scale per 128 x 128 block
+ *                ("Key-value down-projection" page, Linear excerpt, model.py 15 and 179-193); the
+ *                weight used is bf16(e4m3 * scale), dequantised on the device.
+ *   kv_cache     NULL, or [B, cache_len, 512] bf16, 32-byte aligned: positions 0..T-1 receive the
+ *                latent wkv_b consumed (after the FP8 round trip when it is on).
+ *   pe_cache     NULL, or [B, cache_len, 64] bf16, 4-byte aligned: positions 0..T-1 receive k_pe
+ *                as the attention used it (rotated under MLA_FLAG_ROPE).
+ *   cache_len    positions per sequence in the caches; at least T when a cache is given. */
+typedef struct {
+  unsigned flags;
+  int32_t* n_keys;
+  const float* wkv_b_scale;
+  mla_bf16* kv_cache;
+  mla_bf16* pe_cache;
+  int32_t cache_len;
+} mla_prefill_options;
+
+/* Workspace bytes of mla_sparse_prefill_opt (0 if `d` or `opt` is invalid; opt may be NULL):
+ * mla_sparse_prefill_workspace_size(d) plus, with FP8 weights, the dequantised wkv_b (H*256*512
+ * bf16) and, under MLA_FLAG_ROPE, the (cos, sin) table [T, 32] fp32 pairs and the rotated k_pe
+ * [B, T, 64] bf16, each 1024-byte aligned. */
+MLA_API size_t mla_sparse_prefill_opt_workspace_size(mla_dims d, const mla_prefill_options* opt);
+
+/* mla_sparse_prefill with the options above (opt may be NULL: then it is mla_sparse_prefill).
+ * wkv_b points at bf16 or, when opt->wkv_b_scale is set, at e4m3 bytes. The workspace rules are
+ * mla_sparse_prefill's, with mla_sparse_prefill_opt_workspace_size. */
+MLA_API mla_status mla_sparse_prefill_opt(const mla_bf16* q, const mla_bf16* c_kv, const mla_bf16* k_pe,
+                                          const float* gamma, const void* wkv_b, const int32_t* topk_idx,
+                                          mla_bf16* out, float* lse, mla_dims d, void* workspace,
+                                          size_t workspace_bytes, void* stream, const mla_prefill_options* opt);
 
 /* Stage 1 alone: the index mask of the MHA prefill excerpt ("Keys" page, model.py 574-589: -inf
  * scattered to 0 at the top-k indices, plus the causal mask), written as canonical selection
@@ -118,7 +185,8 @@ MLA_API mla_status mla_canon_select(const int32_t* topk_idx, mla_dims d, uint32_
  *   kv  [B, H, T, 256] fp16 (IEEE binary16 bit patterns): kv[.., 0:128] = k_hi = fp16(k_nope),
  *       kv[.., 128:256] = fp16(v);
  *   klo [B, H, T, 128] fp8 e4m3 bytes: (k_nope - k_hi) * 2^11, the part of k_nope fp16 drops.
- * k_hi + klo * 2^-11 carries k_nope to about 2^-14 relative. |k_nope|, |v| must stay below 448. */
+ * k_hi + klo * 2^-11 carries k_nope to about 2^-14 relative. |k_nope| >= MLA_MAX_ABS_K_NOPE or
+ * |v| > MLA_MAX_ABS_V records MLA_ERR_RANGE. */
 MLA_API mla_status mla_kvnorm_wkvb(const mla_bf16* c_kv, const float* gamma, const mla_bf16* wkv_b, mla_dims d,
                            uint16_t* kv, uint8_t* klo, void* stream);
 
@@ -129,6 +197,42 @@ MLA_API mla_status mla_kvnorm_wkvb(const mla_bf16* c_kv, const float* gamma, con
 MLA_API mla_status mla_sparse_attention(const mla_bf16* q, const mla_bf16* k_pe, const uint16_t* kv,
                                 const uint8_t* klo, const uint32_t* sel_bits, mla_bf16* out, float* lse,
                                 mla_dims d, void* stream);
+
+/* FP8 block-scaled wkv_b -> its bf16 weight ("Key-value down-projection" page, Linear excerpt,
+ * model.py 15 and 179-193): w[n, c] = bf16(e4m3(w8[n, c]) * scale[n / 128, c / 128]), the product
+ * in fp32, rounded to nearest.
+ *   w8     [rows, 512] e4m3 bytes, 16-byte aligned; rows a multiple of 128 (H*256 for wkv_b).
+ *   scale  [rows / 128, 4] fp32.
+ *   w      [rows, 512] bf16 (written), 32-byte aligned. */
+MLA_API mla_status mla_dequant_wkvb_fp8(const uint8_t* w8, const float* scale, int32_t rows, mla_bf16* w,
+                                        void* stream);
+
+/* Stages 2-3 with the options of mla_prefill_options: as mla_kvnorm_wkvb, plus
+ *   flags     0 or MLA_FLAG_FP8_LATENT (the FP8 round trip of the normalised latent);
+ *   kv_cache  NULL or [B, cache_len, 512] bf16, 32-byte aligned: receives the latent the GEMM
+ *             consumed (positions 0..T-1). */
+MLA_API mla_status mla_kvnorm_wkvb_opt(const mla_bf16* c_kv, const float* gamma, const mla_bf16* wkv_b, mla_dims d,
+                                       uint16_t* kv, uint8_t* klo, unsigned flags, mla_bf16* kv_cache,
+                                       int32_t cache_len, void* stream);
+
+/* YaRN RoPE of k_pe at positions 0..T-1 (see MLA_FLAG_ROPE) and the table the attention stage
+ * rotates q with.
+ *   k_pe      [B, T, 64] bf16, unrotated, 4-byte aligned.
+ *   k_pe_rot  [B, T, 64] bf16 (written), 4-byte aligned.
+ *   rope_cs   [T, 32] pairs of fp32 (cos, sin) of the angle t * f_i (written), 32-byte aligned.
+ *   pe_cache  NULL or [B, cache_len, 64] bf16: receives k_pe_rot. */
+MLA_API mla_status mla_rope_k_pe(const mla_bf16* k_pe, mla_dims d, mla_bf16* k_pe_rot, float* rope_cs,
+                                 mla_bf16* pe_cache, int32_t cache_len, void* stream);
+
+/* The YaRN frequencies f_i (radians per position) of the 32 rotary pairs. Host-only. */
+MLA_API void mla_yarn_frequencies(double* f32_out);
+
+/* Stage 4 with RoPE on q: as mla_sparse_attention, plus rope_cs (NULL, or the table mla_rope_k_pe
+ * wrote): q[..., 128:192] is then unrotated and is rotated at position t inside the stage. k_pe
+ * must be the rotated one. */
+MLA_API mla_status mla_sparse_attention_opt(const mla_bf16* q, const mla_bf16* k_pe, const uint16_t* kv,
+                                            const uint8_t* klo, const uint32_t* sel_bits, mla_bf16* out, float* lse,
+                                            mla_dims d, const float* rope_cs, void* stream);
 
 /* Allocation-free form of mla_sparse_prefill, for callers that cannot allocate device memory
  * when they run the prefill (code inside an allocator or memory-pool callback, engines that fix

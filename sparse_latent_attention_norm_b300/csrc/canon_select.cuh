@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(kCanonThreads) canon_select_kernel(const int32
   const int64_t row = blockIdx.x;
   const int t = static_cast<int>(row % T);
   const int words = (t / 128 + 1) * 4;  // <= W
+  if (!in_bounds(words <= W)) return;
   for (int w = threadIdx.x; w < words; w += kCanonThreads) bits[w] = 0u;
   __syncthreads();
 
@@ -44,14 +45,14 @@ __global__ void __launch_bounds__(kCanonThreads) canon_select_kernel(const int32
       for (int e = 0; e < 4; ++e) {
         const int j = js[e];
         bad |= (j < 0) | (j >= T);
-        if (j >= 0 && j <= t) atomicOr(&bits[j >> 5], 1u << (j & 31));
+        if (j >= 0 && j <= t && in_bounds((j >> 5) < words)) atomicOr(&bits[j >> 5], 1u << (j & 31));
       }
     }
   } else {
     for (int i = threadIdx.x; i < K; i += kCanonThreads) {
       const int j = __ldg(idx + i);
       bad |= (j < 0) | (j >= T);
-      if (j >= 0 && j <= t) atomicOr(&bits[j >> 5], 1u << (j & 31));
+      if (j >= 0 && j <= t && in_bounds((j >> 5) < words)) atomicOr(&bits[j >> 5], 1u << (j & 31));
     }
   }
   if (validate && bad) set_error(kErrIndex);

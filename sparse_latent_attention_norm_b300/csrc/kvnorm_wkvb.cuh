@@ -22,15 +22,14 @@
 // M=128 N=128 K=16 into one of two TMEM accumulators, so a unit's epilogue overlaps the next
 // unit's MMAs. The epilogue converts the accumulator and stores each row straight from registers
 // with 32-byte stores (kv: 256 bytes, klo: 128 bytes per row); staging it in shared memory for
-// TMA stores measured slower. A
-// CTA takes a contiguous range of units, row-tile-major, so it normalises few row tiles. With
-// CLUSTER > 1 the CTAs of a cluster take adjacent row tiles and walk the same units, each
-// loading 1/CLUSTER of every W slice and multicasting it to all, so W leaves L2 once per cluster.
+// TMA stores measured slower. A CTA takes a contiguous range of units, row-tile-major, so it
+// normalises few row tiles.
 //
 // Warp roles (192 threads): warp 0 TMA producer of W, warp 1 TMEM owner + MMA issuer, warps 2-5
 // normalise rows into TMEM and run the epilogue (warp w owns TMEM lanes 32*(w%4) .. +31).
 #pragma once
 
+#include "mla.h"
 #include "ptx.cuh"
 
 namespace mla {
@@ -50,12 +49,6 @@ constexpr int STAGES_PER_UNIT = NKATOM / KPS;
 constexpr int B_STAGE_BYTES = KPS * ATOM_BYTES;
 constexpr int NSTAGE = 4;
 constexpr int THREADS = 192;
-// CTAs per cluster sharing every W slice by multicast (each loads 1/CLUSTER of a slice's rows).
-// 1: measured faster than 2 once stages carry several slices (multicast halves each CTA's loads
-// but also its TMA rate per byte received).
-constexpr int CLUSTER = 1;
-constexpr int B_ROWS_PER_CTA = BN / CLUSTER;    // W rows each CTA of a cluster loads per slice
-constexpr uint16_t CLUSTER_MASK = (1u << CLUSTER) - 1;
 constexpr int TILE_BYTES = NSTAGE * B_STAGE_BYTES;
 static_assert(NKATOM % KPS == 0, "stages split the latent evenly");
 
@@ -82,12 +75,32 @@ struct Params {
   int B, T, H;
   int mt_per_b;            // row tiles per batch: ceil(T / 128)
   int n_mtiles;            // B * mt_per_b
-  int units;               // ceil(n_mtiles / CLUSTER) * H * 2: units of a cluster
+  int units;               // n_mtiles * H * 2
   const uint16_t* c_kv;    // [B, T, 512] bf16
   const float* gamma;      // [512]
   uint16_t* kv_out;        // [B, H, T, 256] fp16
   uint8_t* klo_out;        // [B, H, T, 128] e4m3
+  int fp8_latent;          // 1: the normalised latent goes through the KV cache's FP8 round trip
+  uint16_t* kv_cache;      // [B, cache_len, 512] bf16 or null: receives the latent the GEMM consumes
+  int cache_len;
 };
+
+// One normalised latent value: gamma * (x * r) in fp32, rounded to bf16 (RMSNorm excerpt).
+__device__ __forceinline__ float norm_value(float x, float r, float g) { return __fmul_rn(g, __fmul_rn(x, r)); }
+
+// Two bf16 values (low, high half of w) -> two e4m3 codes of (value / scale), rounded to nearest
+// (satfinite), -> the dequantised values e4m3 * scale in fp32, rounded to bf16: the KV cache's
+// FP8 round trip of one pair ("Keys" page, KV-cache excerpt: act_quant in blocks of 128, then
+// fp8 * scale cast back to bf16).
+__device__ __forceinline__ uint32_t fp8_round_trip_bf16x2(uint32_t w, float scale) {
+  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
+  const uint16_t q2 = pack_e4m3x2(__fdiv_rn(lo, scale), __fdiv_rn(hi, scale));
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(q2));   // exact: e4m3 values are fp16 values
+  const float qlo = f16_bits_to_float(static_cast<uint16_t>(h2 & 0xFFFFu));
+  const float qhi = f16_bits_to_float(static_cast<uint16_t>(h2 >> 16));
+  return pack_bf16x2(__fmul_rn(qlo, scale), __fmul_rn(qhi, scale));
+}
 
 // Named barrier of the epilogue warps that also ANDs `pred` over their 128 threads.
 __device__ __forceinline__ bool epi_sync_and(bool pred) {
@@ -101,7 +114,7 @@ __device__ __forceinline__ bool epi_sync_and(bool pred) {
   return r != 0;
 }
 
-__global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, 1)
     kvnorm_wkvb_kernel(const __grid_constant__ CUtensorMap tm_w, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {
@@ -122,15 +135,10 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
   const int warp = warp_id();
   const int lane = lane_id();
 
-  // The CTAs of a cluster take adjacent row tiles and walk the same units (head, half), so each W
-  // slice is read from L2 once per cluster: every CTA loads 1/CLUSTER of its rows and multicasts
-  // them to the whole cluster. Contiguous range of cluster units: u -> row-tile group u / (2H),
-  // head (u / 2) % H, half u % 2; this CTA's row tile is group * CLUSTER + rank.
-  const int rank = static_cast<int>(cluster_ctarank());
-  const int G = gridDim.x / CLUSTER;
-  const int cl = blockIdx.x / CLUSTER;
-  const int u_begin = static_cast<int>((static_cast<int64_t>(p.units) * cl) / G);
-  const int u_end = static_cast<int>((static_cast<int64_t>(p.units) * (cl + 1)) / G);
+  // Contiguous range of units per CTA: u -> row tile u / (2H), head (u / 2) % H, half u % 2.
+  const int G = gridDim.x;
+  const int u_begin = static_cast<int>((static_cast<int64_t>(p.units) * blockIdx.x) / G);
+  const int u_end = static_cast<int>((static_cast<int64_t>(p.units) * (blockIdx.x + 1)) / G);
 
   if (threadIdx.x == 0) {
     ctl.abort_flag = 0;
@@ -138,8 +146,8 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
     mbar_init(&a_ready, 128);
     mbar_init(&drain, 1);
     for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(&b_full[s], 1);              // own producer's expect_tx; bytes from every CTA's part
-      mbar_init(&b_empty[s], CLUSTER);       // one commit from each CTA's MMA issuer
+      mbar_init(&b_full[s], 1);              // the producer's expect_tx
+      mbar_init(&b_empty[s], 1);             // the MMA issuer's commit
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&acc_full[s], 1);
@@ -157,14 +165,11 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // every CTA's barriers are initialised before any multicast copy or commit reaches them
-  cluster_sync_all();
   const uint32_t tmem = ctl.tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer: this CTA's part of every W slice
-    // A stage is refilled once every CTA of the cluster has consumed it (b_empty counts one commit
-    // per CTA); the own b_full expects the whole stage, whose parts arrive from every CTA.
+    // ------------------------------------------------ TMA producer: W slices
+    // A stage is refilled once the MMAs that read it have completed (b_empty).
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -177,12 +182,12 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
           if (!mbar_wait(&b_empty[stage], phase ^ 1, abort_p)) { ok = false; break; }
           mbar_arrive_expect_tx(&b_full[stage], B_STAGE_BYTES);
           for (int a = 0; a < KPS; ++a) {
-            uint8_t* dst = sB + stage * B_STAGE_BYTES + a * ATOM_BYTES + rank * B_ROWS_PER_CTA * 128;
-            const int x = (sk * KPS + a) * KATOM, y = h * 256 + half * BN + rank * B_ROWS_PER_CTA;
-            if constexpr (CLUSTER > 1)
-              tma_load_2d_multicast(dst, &tm_w, &b_full[stage], x, y, CLUSTER_MASK);
-            else
+            uint8_t* dst = sB + stage * B_STAGE_BYTES + a * ATOM_BYTES;
+            const int x = (sk * KPS + a) * KATOM, y = h * 256 + half * BN;
+            if (in_bounds(x + KATOM <= KDIM && y + BN <= p.H * 256))
               tma_load_2d(dst, &tm_w, &b_full[stage], x, y);
+            else
+              mbar_complete_tx(&b_full[stage], ATOM_BYTES);
           }
           pending[stage] = true;
           pend_parity[stage] = phase;
@@ -230,10 +235,7 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
                       idesc, (ka | k4) != 0 ? 1u : 0u);
             }
           issued = true;
-          if constexpr (CLUSTER > 1)
-            umma_commit_multicast(&b_empty[stage], CLUSTER_MASK);
-          else
-            umma_commit(&b_empty[stage]);
+          umma_commit(&b_empty[stage]);
           if (++stage == NSTAGE) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -258,9 +260,8 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int u = u_begin; u < u_end; ++u) {
-      const int m = (u / (2 * p.H)) * CLUSTER + rank, h = (u >> 1) % p.H, half = u & 1;
-      const bool active = m < p.n_mtiles;   // the last group may have fewer row tiles than CTAs
-      const int b = active ? m / p.mt_per_b : 0, t0 = active ? (m % p.mt_per_b) * BM : 0;
+      const int m = u / (2 * p.H), h = (u >> 1) % p.H, half = u & 1;
+      const int b = m / p.mt_per_b, t0 = (m % p.mt_per_b) * BM;
       if (m != cur_m) {
         // RMSNorm of row (b, t0 + r) into TMEM once the previous tile's MMAs are done with y
         if (seg > 0) ok = __all_sync(0xffffffffu, mbar_wait(&a_free, (seg - 1) & 1, abort_p));
@@ -268,7 +269,7 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
         if (!ok) break;
         tc_fence_after();
         const int t = t0 + r;
-        const bool valid = active && t < p.T;
+        const bool valid = t < p.T && in_bounds(b < p.B);
         const uint4* row = reinterpret_cast<const uint4*>(p.c_kv + (static_cast<int64_t>(b) * p.T + (valid ? t : 0)) * KDIM);
         // sum of squares in ascending feature order; the row's 16-byte loads go out 8 at a
         // time (the tile's rows usually come from DRAM: eight round trips instead of sixteen)
@@ -292,9 +293,8 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
         }
         const float var = __fmul_rn(ss, 1.0f / KDIM);   // exact: division by a power of two
         const float rinv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, RMS_EPS)));
-#pragma unroll 1
-        for (int cc = 0; cc < KDIM / 64; ++cc) {   // 64 features -> 32 TMEM columns
-          uint32_t o[32];
+        // y of 64 features of the row (chunk cc) as 32 bf16 pairs
+        auto norm_chunk = [&](int cc, uint32_t (&o)[32]) {
 #pragma unroll
           for (int a = 0; a < 8; ++a) {
             const uint4 v = valid ? __ldg(row + cc * 8 + a) : make_uint4(0, 0, 0, 0);
@@ -306,10 +306,51 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
             for (int e = 0; e < 4; ++e) {
               const float lo = __uint_as_float(w[e] << 16);
               const float hi = __uint_as_float(w[e] & 0xFFFF0000u);
-              o[a * 4 + e] = pack_bf16x2(__fmul_rn(g[2 * e], __fmul_rn(lo, rinv)), __fmul_rn(g[2 * e + 1], __fmul_rn(hi, rinv)));
+              o[a * 4 + e] = pack_bf16x2(norm_value(lo, rinv, g[2 * e]), norm_value(hi, rinv, g[2 * e + 1]));
             }
           }
-          tmem_st_32x32b_x32(lane_addr + TM_A + static_cast<uint32_t>(cc * 32), o);
+        };
+        uint16_t* cache_row = (p.kv_cache != nullptr && valid)
+                                  ? p.kv_cache + (static_cast<int64_t>(b) * p.cache_len + t) * KDIM
+                                  : nullptr;
+        if (!p.fp8_latent) {
+#pragma unroll 1
+          for (int cc = 0; cc < KDIM / 64; ++cc) {   // 64 features -> 32 TMEM columns
+            uint32_t o[32];
+            norm_chunk(cc, o);
+            tmem_st_32x32b_x32(lane_addr + TM_A + static_cast<uint32_t>(cc * 32), o);
+            if (cache_row)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) stg_v8(cache_row + cc * 64 + k * 16, *reinterpret_cast<const uint32_t(*)[8]>(&o[8 * k]));
+          }
+        } else {
+          // per block of 128 features: the block's max |y| (first pass), then y again, its FP8
+          // round trip with scale = max / 448 (1 for an all-zero block) into TMEM (second pass)
+#pragma unroll 1
+          for (int blk = 0; blk < KDIM / 128; ++blk) {
+            float amax = 0.f;
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+              uint32_t o[32];
+              norm_chunk(blk * 2 + half, o);
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(o[e] << 16)), fabsf(__uint_as_float(o[e] & 0xFFFF0000u))));
+            }
+            const float scale = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+              const int cc = blk * 2 + half;
+              uint32_t o[32];
+              norm_chunk(cc, o);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = fp8_round_trip_bf16x2(o[e], scale);
+              tmem_st_32x32b_x32(lane_addr + TM_A + static_cast<uint32_t>(cc * 32), o);
+              if (cache_row)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) stg_v8(cache_row + cc * 64 + k * 16, *reinterpret_cast<const uint32_t(*)[8]>(&o[8 * k]));
+            }
+          }
         }
         tmem_st_wait();
         tc_fence_before();
@@ -336,7 +377,15 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
       ok = epi_sync_and(got);
       if (!ok) break;
       const int t_row = t0 + r;
-      if (active && t_row < p.T) {
+      if (t_row < p.T) {
+        // range of the values carried exactly: the e4m3 residual of k_nope saturates from 512 on,
+        // v is stored in fp16 (NaN counts as out of range)
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < BN; ++i) amax = max_nan(amax, fabsf(__uint_as_float(v[i])));
+        if (!(half == 0 ? amax < MLA_MAX_ABS_K_NOPE : amax <= MLA_MAX_ABS_V)) set_error(kErrRange);
+      }
+      if (t_row < p.T && in_bounds(b < p.B && h < p.H)) {
         const int64_t prow = (static_cast<int64_t>(b) * p.H + h) * p.T + t_row;
         uint32_t hw[BN / 2];
 #pragma unroll
@@ -370,8 +419,6 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
         }
       }
     }
-    // the stores read shared memory until they complete: wait before the CTA exits
-
   }
 
   tc_fence_before();
@@ -380,8 +427,6 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
-  // no CTA leaves while another CTA's multicast commits may still arrive on its barriers
-  cluster_sync_all();
 }
 
 }  // namespace k1

@@ -42,6 +42,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// Complete `bytes` of the barrier's expected transaction count without a copy (the checked
+// build's stand-in for a TMA load it skipped, so the barrier still completes).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -60,6 +65,29 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr unsigned kErrTimeout = 5;
 // Recorded when a kernel finds its dynamic shared memory less aligned than its tiles need.
 constexpr unsigned kErrUnsupportedLayout = 2;
+// Recorded when a value leaves the range the kernels carry exactly (MLA_ERR_RANGE).
+constexpr unsigned kErrRange = 7;
+// Recorded by the checked build (MLA_CHECKS) when an index or coordinate is out of bounds.
+constexpr unsigned kErrBounds = 8;
+
+// Bounds check of the checked build: with MLA_CHECKS defined, `in_bounds(ok)` records
+// MLA_ERR_BOUNDS when `ok` is false and returns it, so the caller skips the access; without it
+// the check compiles to `true`. No check traps: the kernel carries on with the access skipped.
+#ifdef MLA_CHECKS
+__device__ __forceinline__ bool in_bounds(bool ok) {
+  if (!ok) set_error(kErrBounds);
+  return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(bool) { return true; }
+#endif
+
+// max(a, b) that returns NaN when either operand is NaN (fmaxf would drop it).
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
 
 // Bounded wait on phase `parity`. Returns false (after recording a timeout) when the limit
 // passes, or at once when `abort_flag` (shared, may be null) is already set by another thread.
@@ -94,16 +122,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
-      : "memory");
-}
-// The same box written to the same shared-memory offset of every CTA in `cta_mask` (this cluster),
-// each of whose mbarriers at `bar`'s offset receives the bytes that landed in that CTA.
-__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
-                                                      uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask)
       : "memory");
 }
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
@@ -189,25 +207,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
-}
-
-// As umma_commit, arriving once on the mbarrier at `bar`'s offset in every CTA of `cta_mask`.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
-// Thread-block cluster: rank of this CTA and a barrier over all threads of the cluster.
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets row (lane base + i).

@@ -19,7 +19,8 @@
 //   softmax: four threads per query row (TMEM lane), 32 key columns each: apply the row's
 //           selection bits, block max of the raw scores (combined across the four threads with
 //           shared atomicMax), running max in the log2 domain with lazy rescaling (only when the
-//           max grows by more than 2^8), p = 2^(s * scale * log2 e - m) evaluated in fp16
+//           max grows by more than 8 log2 units, with an exact power-of-two shift of the block's
+//           exponents in between), p = 2^(s * scale * log2 e - m) evaluated in fp16
 //           (ex2.approx.f16x2) and written to TMEM (64 cols of fp16 pairs).
 //   PV    : O[128 x 128] += P[128 x 128] . V[128 x 128], 8 UMMAs kind::f16 with P (fp16) read
 //           from TMEM and V (fp16) from shared memory (MN-major), O in TMEM (128 cols).
@@ -39,6 +40,7 @@
 // rows, and key / value columns 32*((w-2)/4) .. +31).
 #pragma once
 
+#include "mla.h"
 #include "ptx.cuh"
 
 namespace mla {
@@ -84,7 +86,15 @@ constexpr uint32_t TM_S = 0;            // S buffers at cols 0 and 128
 constexpr uint32_t TM_O = 256;          // O at cols 256..383
 constexpr uint32_t TM_QN = 384;         // q_nope as fp16 pairs, cols 384..447
 constexpr uint32_t TM_P = 448;          // P as fp16 pairs, cols 448..511
-constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
+// Online softmax in the log2 domain against a lagging reference max m. O and l are rescaled
+// (a TMEM round trip of O) only when a block's max exceeds m by more than RESCALE_THRESHOLD log2
+// units. Between rescales a block's exponents x = s * scale * log2 e - m can reach 8, where fp16
+// x carries an absolute error up to 2^-9 (1.4e-3 nats of lse on a row that one key carries). So
+// each row also takes an integer shift c >= 0 that brings x - c to at most X_MAX: p = 2^(x - c)
+// in fp16 (x - c with absolute error <= 2^-12, p with relative error <= 2^-11: lse within about
+// 7e-4 nats), then P = p * 2^c, exact in fp16 (an exponent shift), so P and l stay relative to m.
+constexpr float RESCALE_THRESHOLD = 8.0f;
+constexpr float X_MAX = 1.0f;
 constexpr float Q8_SCALE = 1.0f / 2048.0f; // 2^-11, undoes the 2^11 on k_lo
 
 struct Params {
@@ -98,6 +108,8 @@ struct Params {
   const uint32_t* sel_bits;
   uint16_t* out;           // [B, T, H, 128] bf16
   float* lse;              // [B, T, H]
+  const float2* rope_cs;   // null, or [T, 32] (cos, sin): q[..., 128:192] is unrotated and gets YaRN
+                           // RoPE at position t here (pairs (2i, 2i+1), fp32, no fused multiply-add)
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -111,6 +123,13 @@ __device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
   uint32_t y;
   asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
   return y;
+}
+
+// Elementwise product of two fp16 pairs, rounded to nearest.
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
 }
 
 // acc + lo(h) + hi(h): both fp16 halves of `h` added to an fp32 accumulator in fp32.
@@ -290,8 +309,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         // q_pe of this tile replaces the previous tile's once its last QK^T has completed
         if (it >= 1 && !mbar_wait(&q_free, (it - 1) & 1, abort_p)) { ok = false; break; }
         qpend = false;
-        mbar_arrive_expect_tx(&q_full, QPE_BYTES);
-        tma_load_4d(sQpe, &tm_q, &q_full, 128, tl.h, tl.t0, tl.b);
+        if (p.rope_cs != nullptr) {
+          // the query warps rotate q_pe into sQpe themselves (prepare_queries)
+          mbar_arrive(&q_full);
+        } else {
+          mbar_arrive_expect_tx(&q_full, QPE_BYTES);
+          if (in_bounds(tl.h < p.H && tl.t0 < p.T && tl.b < p.B))
+            tma_load_4d(sQpe, &tm_q, &q_full, 128, tl.h, tl.t0, tl.b);
+          else
+            mbar_complete_tx(&q_full, QPE_BYTES);
+        }
         qpend = true;
         qpar = it & 1;
         for (int i = 0; i < tl.nblk; ++i) {
@@ -299,10 +326,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           uint8_t* kdst = sK + ks * K_BYTES;
           const int j0 = i * BK;
           mbar_arrive_expect_tx(&k_full[ks], K_BYTES);
-          tma_load_3d(kdst, &tm_kv, &k_full[ks], 0, j0, kv_plane);
-          tma_load_3d(kdst + ATOM_BYTES, &tm_kv, &k_full[ks], 64, j0, kv_plane);
-          tma_load_3d(kdst + 2 * ATOM_BYTES, &tm_kpe, &k_full[ks], 0, j0, tl.b);
-          tma_load_3d(kdst + 3 * ATOM_BYTES, &tm_klo, &k_full[ks], 0, j0, kv_plane);
+          if (in_bounds(j0 < p.T && kv_plane < p.B * p.H)) {
+            tma_load_3d(kdst, &tm_kv, &k_full[ks], 0, j0, kv_plane);
+            tma_load_3d(kdst + ATOM_BYTES, &tm_kv, &k_full[ks], 64, j0, kv_plane);
+            tma_load_3d(kdst + 2 * ATOM_BYTES, &tm_kpe, &k_full[ks], 0, j0, tl.b);
+            tma_load_3d(kdst + 3 * ATOM_BYTES, &tm_klo, &k_full[ks], 0, j0, kv_plane);
+          } else {
+            mbar_complete_tx(&k_full[ks], K_BYTES);
+          }
           kpend[ks] = true;
           kpar[ks] = kph;
           if (++ks == NK_STAGE) { ks = 0; kph ^= 1; }
@@ -343,8 +374,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           uint8_t* vdst = sV + vs * V_BYTES;
           const int j0 = i * BK;
           mbar_arrive_expect_tx(&v_full[vs], V_BYTES);
-          tma_load_3d(vdst, &tm_kv, &v_full[vs], 128, j0, kv_plane);
-          tma_load_3d(vdst + ATOM_BYTES, &tm_kv, &v_full[vs], 192, j0, kv_plane);
+          if (in_bounds(j0 < p.T && kv_plane < p.B * p.H)) {
+            tma_load_3d(vdst, &tm_kv, &v_full[vs], 128, j0, kv_plane);
+            tma_load_3d(vdst + ATOM_BYTES, &tm_kv, &v_full[vs], 192, j0, kv_plane);
+          } else {
+            mbar_complete_tx(&v_full[vs], V_BYTES);
+          }
           vpend[vs] = true;
           vpar[vs] = vph;
           if (++vs == NV_STAGE) { vs = 0; vph ^= 1; }
@@ -479,9 +514,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t qn[16];
       uint32_t q8[8];
       uint32_t qw[2][8];   // this part's 32 q_nope features: two 32-byte loads
+      float amax = 0.f;    // largest |q_nope| of the part (NaN propagates): fp16 must hold it
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        if (row_valid) ldg_v8(qrow + part * 4 + 2 * c, qw[c]);
+        if (row_valid && in_bounds(tl.b < p.B && tl.h < p.H)) ldg_v8(qrow + part * 4 + 2 * c, qw[c]);
 #pragma unroll
         for (int e = 0; e < 8; ++e)
           if (!row_valid) qw[c][e] = 0u;
@@ -494,6 +530,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int e = 0; e < 4; ++e) {
           const float lo = __uint_as_float(w[e] << 16);
           const float hi = __uint_as_float(w[e] & 0xFFFF0000u);
+          amax = max_nan(amax, max_nan(fabsf(lo), fabsf(hi)));
           qn[c * 4 + e] = pack_f16x2(lo, hi);
           const uint32_t b8 = pack_e5m2x2(lo * Q8_SCALE, hi * Q8_SCALE);
           if (e & 1)
@@ -502,12 +539,41 @@ __global__ void __launch_bounds__(THREADS, 1)
             q8[c * 2 + (e >> 1)] = b8;
         }
       }
+      if (!(amax <= MLA_MAX_ABS_Q_NOPE)) set_error(kErrRange);
       tmem_st_32x32b_x16(tmem + lane_off + TM_QN + part * 16, qn);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int chunk = part * 2 + c;   // 16-byte chunk = 16 e5m2 values
         *reinterpret_cast<uint4*>(sQ8 + r * 128 + ((chunk ^ (r & 7)) * 16)) =
             make_uint4(q8[c * 4], q8[c * 4 + 1], q8[c * 4 + 2], q8[c * 4 + 3]);
+      }
+      if (p.rope_cs != nullptr) {
+        // q_pe features 16*part .. +15 (pairs 8*part .. +7) rotated at position t into the
+        // swizzled q_pe tile (16-byte chunk c of row r at c ^ (r & 7)), as the TMA copy would
+        // have placed the rotated values
+        uint32_t x[8], o[8];
+        uint32_t csw[2][8];
+        if (row_valid && in_bounds(tl.b < p.B && tl.h < p.H)) {
+          ldg_v8(qrow + 16 + part * 2, x);
+          const float2* crow = p.rope_cs + static_cast<int64_t>(t) * 32 + part * 8;
+          ldg_v8(crow, csw[0]);
+          ldg_v8(crow + 4, csw[1]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float c = __uint_as_float(csw[e >> 2][(e & 3) * 2]), sn = __uint_as_float(csw[e >> 2][(e & 3) * 2 + 1]);
+            const float a = __uint_as_float(x[e] << 16), bb = __uint_as_float(x[e] & 0xFFFF0000u);
+            o[e] = pack_bf16x2(__fsub_rn(__fmul_rn(a, c), __fmul_rn(bb, sn)), __fadd_rn(__fmul_rn(a, sn), __fmul_rn(bb, c)));
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = 0u;
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int chunk = part * 2 + c;
+          *reinterpret_cast<uint4*>(sQpe + r * 128 + ((chunk ^ (r & 7)) * 16)) =
+              make_uint4(o[c * 4], o[c * 4 + 1], o[c * 4 + 2], o[c * 4 + 3]);
+        }
       }
       tmem_st_wait();
       fence_proxy_async_smem();
@@ -527,7 +593,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (ok && item >= 0) {
       const Tile t0l = tile_of(item, p);
       const int tt = t0l.t0 + r;
-      first_mask = (tt < p.T) ? __ldg(p.sel_bits + (static_cast<int64_t>(t0l.b) * p.T + tt) * p.W + part) : 0u;
+      first_mask = (tt < p.T && in_bounds(t0l.b < p.B)) ? __ldg(p.sel_bits + (static_cast<int64_t>(t0l.b) * p.T + tt) * p.W + part) : 0u;
       prepare_queries(t0l);
     }
     while (ok && item >= 0) {
@@ -542,7 +608,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t mask_next = first_mask;
       for (int i = 0; i < tl.nblk; ++i, ++g) {
         const uint32_t mask = mask_next;
-        if (i + 1 < tl.nblk) mask_next = row_valid ? __ldg(bits_row + (i + 1) * 4) : 0u;
+        if (i + 1 < tl.nblk)
+          mask_next = (row_valid && in_bounds((i + 1) * 4 + part < p.W && tl.b < p.B)) ? __ldg(bits_row + (i + 1) * 4) : 0u;
         const int sb = g & 1;
         const int slot = g % 3;
         bool got = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (g >> 1) & 1, abort_p));
@@ -591,17 +658,28 @@ __global__ void __launch_bounds__(THREADS, 1)
         const float alpha = need_o ? ex2(m_ref - mb) : 1.0f;
         if (need_o) l *= alpha;
         if (need) m_ref = mb;
-        const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;   // no key yet: every p is 0
-        // p = 2^x with x = s * scale * log2 e - m <= 8 rounded to fp16 and exponentiated two at a
+        // integer shift of this row's exponents (0 after a rescale and while no key is selected);
+        // mb <= m_ref + RESCALE_THRESHOLD here, so 0 <= c <= RESCALE_THRESHOLD - X_MAX = 7
+        const float c_shift = (mb == -INFINITY || m_ref == -INFINITY) ? 0.f : fmaxf(0.f, ceilf(mb - m_ref - X_MAX));
+        const float neg_m = (m_ref == -INFINITY) ? 0.f : -(m_ref + c_shift);   // no key yet: every p is 0
+        // p = 2^x with x = s * scale * log2 e - m - c <= 1 rounded to fp16 and exponentiated two at a
         // time in fp16 (P is consumed as fp16 by the PV UMMA); l sums the same fp16 values in
         // fp32, so out = O / l divides by exactly the weights O was built from.
         uint32_t pk[PCOLS / 2];
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < PCOLS / 2; ++c) {
+        for (int c = 0; c < PCOLS / 2; ++c)
           pk[c] = ex2_f16x2(pack_f16x2(fmaf(s[2 * c], sl2, neg_m), fmaf(s[2 * c + 1], sl2, neg_m)));
-          ls[c & 3] = add_f16x2_to_f32(pk[c], ls[c & 3]);
+        if (__any_sync(0xffffffffu, c_shift > 0.f)) {
+          // P = p * 2^c: 2^c (c <= 7) is exact in fp16 and so is the product (an exponent shift;
+          // p <= 2, so P <= 256)
+          const uint32_t two_c = pack_f16x2(__int_as_float((127 + static_cast<int>(c_shift)) << 23),
+                                            __int_as_float((127 + static_cast<int>(c_shift)) << 23));
+#pragma unroll
+          for (int c = 0; c < PCOLS / 2; ++c) pk[c] = hmul2_bits(pk[c], two_c);
         }
+#pragma unroll
+        for (int c = 0; c < PCOLS / 2; ++c) ls[c & 3] = add_f16x2_to_f32(pk[c], ls[c & 3]);
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         if (i > 0) {
           // P's TMEM columns and O are free once PV(g-1) has completed (for a tile's first block
@@ -640,7 +718,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int nt_t = nt.t0 + r;
         // the next tile's first selection word, loaded now so its latency passes during the
         // query preparation and this tile's epilogue
-        first_mask = (nt_t < p.T) ? __ldg(p.sel_bits + (static_cast<int64_t>(nt.b) * p.T + nt_t) * p.W + part) : 0u;
+        first_mask = (nt_t < p.T && in_bounds(nt.b < p.B)) ? __ldg(p.sel_bits + (static_cast<int64_t>(nt.b) * p.T + nt_t) * p.W + part) : 0u;
         prepare_queries(nt);
       }
 
@@ -667,7 +745,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float lt = (__uint_as_float(lp[0]) + __uint_as_float(lp[1])) +
                        (__uint_as_float(lp[2]) + __uint_as_float(lp[3]));   // same order in every part
       const float inv_l = (lt > 0.f) ? 1.0f / lt : 0.f;
-      if (row_valid) {
+      if (row_valid && in_bounds(tl.b < p.B && tl.h < p.H)) {
         // this part's 32 output features = 64 bytes, as two 32-byte stores (each store instruction
         // of the warp touches one line per row, so fewer, wider stores take fewer L1 passes)
         uint16_t* orow = p.out + ((static_cast<int64_t>(tl.b) * p.T + t) * p.H + tl.h) * 128 + part * PCOLS;

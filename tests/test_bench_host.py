@@ -83,3 +83,15 @@ def test_source_hash_ignores_comments_not_code():
     c = bench._code_only("int x = 2; // one\nfloat y;\n")
     assert a == b == "intx=1;floaty;"
     assert c != a
+
+
+def test_hardware_mma_flops_headline():
+    # attention: 528 causal key blocks per head (32 query tiles), 24 UMMAs of 128x128x16 each
+    gemm, attn = bench.hardware_mma_flops(1, 4096, 128)
+    assert attn == 128 * 528 * 24 * 2 * 128 * 128 * 16            # 850.4 GF
+    assert gemm == 32 * 128 * 2 * 32 * 2 * 128 * 128 * 16           # 137.4 GF, the formula's up-projection
+    up, _ = bench.formula_flops(1, 4096, 128, 6292480)
+    assert gemm == up
+    # a ragged tail pads the last tile to 128 rows
+    g2, a2 = bench.hardware_mma_flops(2, 130, 3)
+    assert a2 == 2 * 3 * 3 * 24 * 2 * 128 * 128 * 16 and g2 == 2 * 2 * 3 * 2 * 32 * 2 * 128 * 128 * 16

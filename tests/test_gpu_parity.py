@@ -1,8 +1,7 @@
 """Parity of the CUDA path (through the C ABI) with the fp64 oracle, on seeded inputs.
 
-Small and ragged shapes are compared on every output element; the full-size workloads (at the
-launch configuration the benchmark times) on sampled query rows that the oracle computes one by
-one. Tolerances are in tests/parity.py.
+Every output element is compared, on small and ragged shapes and on the full-size workloads at
+the launch configuration the benchmark times. Tolerances are in tests/parity.py.
 """
 
 import numpy as np
@@ -72,12 +71,139 @@ FULL = ["dense_causal", "headline", "stress", "long_context"]
 
 
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled_rows(mla, oracle_lib, name):
+def test_full_size_every_element(mla, oracle_lib, name):
+    # the full-size workloads at the launch configuration the benchmark times, compared with the
+    # oracle on every query row and head (the oracle runs in head groups to bound host memory)
     w = mi.WORKLOADS[name]
     inp = mi.make_inputs(w)
-    rows = parity.sample_rows(w.B, w.T, w.K, n_random=16, seed=w.seed_id)
-    heads = (0, 16) if name == "long_context" else None
-    run_and_compare(mla, oracle_lib, inp, rows=rows, heads=heads, what=name)
+    d = to_dev(inp)
+    B, T, H = w.B, w.T, w.H
+    out, lse, nk = mla.sparse_prefill(d["q"], d["c_kv"], d["k_pe"], d["gamma"], d["wkv_b"], d["topk_idx"],
+                                      n_keys=True)
+    torch.cuda.synchronize()
+    assert mla.get_status() == 0
+    del d
+    og = out.view(B * T, H, 128)
+    lg = lse.view(B * T, H).cpu().numpy()
+    nk = nk.cpu().numpy().reshape(-1)
+    group = 16 if B * T * H > (1 << 22) else H
+    for h0 in range(0, H, group):
+        h1 = min(H, h0 + group)
+        ref_out, ref_lse, ref_n = oracle_lib.prefill(inp, heads=(h0, h1))
+        if h0 == 0:
+            assert np.array_equal(nk, ref_n), f"{name}: n_keys differ"
+        parity.compare(og[:, h0:h1].float().cpu().numpy(), lg[:, h0:h1], ref_out, ref_lse, f"{name} heads {h0}..{h1 - 1}")
+        del ref_out, ref_lse
+
+
+def lazy_rescale_inputs(T=256, H=128, K=16):
+    """Rows whose softmax sits on one key that scores well above the first key block's maximum,
+    with |lse| near or below 1: the score tail of q (feature 128) is b_h for head h and q's first
+    128 features are 0, so score_j = scale * b_h * a_j with a_j the first rotary feature of key j.
+    Keys 0..7 (first key block) have a_j = -1; key t >= 128 has a_t swept over [0, 1]; query t >= 128
+    selects {0..7, t}. Over the heads and rows, the gap between the dominant score and the first
+    block's maximum sweeps about 1 to 16 log2 units, crossing the online softmax's rescale point."""
+    w = mi.custom("lazy_rescale", 1, T, H, K, "uniform", seed_id=210)
+    inp = mi.make_inputs(w)
+    q = torch.zeros((1, T, H, 192), dtype=torch.float32)
+    b = torch.linspace(5.0, 40.0, H)
+    q[0, :, :, 128] = b[None, :]
+    k_pe = torch.zeros((1, T, 64), dtype=torch.float32)
+    k_pe[0, :128, 0] = -1.0
+    k_pe[0, 128:, 0] = torch.linspace(0.0, 1.0, T - 128)
+    topk = np.full((1, T, K), -1, dtype=np.int32)
+    for t in range(T):
+        early = [j for j in range(8) if j <= t]
+        row = early + ([t] if t >= 128 else [])
+        topk[0, t, :len(row)] = row
+    inp["q"] = q.to(torch.bfloat16)
+    inp["k_pe"] = k_pe.to(torch.bfloat16)
+    inp["topk_idx"] = torch.from_numpy(topk)
+    return inp
+
+
+def test_lse_rows_dominated_by_a_late_key(mla, oracle_lib):
+    # the online softmax keeps a reference maximum that lags the true one until a block's maximum
+    # exceeds it by the rescale threshold; a dominant late key then carries the whole row sum, so
+    # the precision of its weight is the precision of lse ("Keys" page, MHA prefill: softmax over
+    # the masked scores; lse is its log normaliser)
+    inp = lazy_rescale_inputs()
+    res = run_and_compare(mla, oracle_lib, inp, what="lazy rescale rows")
+    assert res["rows"] == 256
+
+
+def test_out_of_range_values_are_reported(mla):
+    w = mi.custom("range", 1, 200, 2, 16, "uniform", seed_id=211)
+    inp = mi.make_inputs(w)
+    mla.clear_status()
+    # gamma x 256 makes |k_nope| reach several hundred standard deviations' worth: above 512
+    d = to_dev(dict(inp, gamma=inp["gamma"] * 256.0))
+    mla.sparse_prefill(d["q"], d["c_kv"], d["k_pe"], d["gamma"], d["wkv_b"], d["topk_idx"])
+    assert mla.get_status() == 7                    # MLA_ERR_RANGE
+    mla.clear_status()
+    # one q_nope feature beyond fp16's range
+    q = inp["q"].clone()
+    q[0, 17, 1, 5] = 70144.0                        # a bf16 value above 65504
+    d = to_dev(dict(inp, q=q))
+    mla.sparse_prefill(d["q"], d["c_kv"], d["k_pe"], d["gamma"], d["wkv_b"], d["topk_idx"])
+    assert mla.get_status() == 7
+    mla.clear_status()
+    # the same inputs within range report nothing
+    d = to_dev(inp)
+    mla.sparse_prefill(d["q"], d["c_kv"], d["k_pe"], d["gamma"], d["wkv_b"], d["topk_idx"])
+    assert mla.get_status() == 0
+
+
+def test_checked_build_matches_and_reports_nothing(mla):
+    # libmla_checks.so (compiled with MLA_CHECKS: every gather index, TMA coordinate and output
+    # row checked before use) gives the same bits as libmla.so and records no failed check
+    import ctypes
+    from sparse_latent_attention_norm_b300 import build
+    Lc = mla.load(build.build(checks=True))
+    assert Lc.mla_clear_status() == 0
+    for w in [mi.custom("checked_a", 2, 333, 5, 48, "uniform", seed_id=212),
+              mi.custom("checked_b", 1, 700, 3, 96, "clustered", recent=256, stress=True, seed_id=213)]:
+        d = to_dev(mi.make_inputs(w))
+        out, lse = mla.sparse_prefill(d["q"], d["c_kv"], d["k_pe"], d["gamma"], d["wkv_b"], d["topk_idx"])
+        out2 = torch.empty_like(out)
+        lse2 = torch.empty_like(lse)
+        P = ctypes.c_void_p
+        rc = Lc.mla_sparse_prefill_ex(*[P(d[k].data_ptr()) for k in ("q", "c_kv", "k_pe", "gamma", "wkv_b", "topk_idx")],
+                                      P(out2.data_ptr()), P(lse2.data_ptr()), mla.Dims(w.B, w.T, w.H, w.K), None, 0,
+                                      P(torch.cuda.current_stream().cuda_stream), None, 0)
+        assert rc == 0
+        torch.cuda.synchronize()
+        assert Lc.mla_get_status() == 0
+        assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def test_prefill_captured_in_a_cuda_graph(mla):
+    # all stages run on the caller's stream, so a call captures into a CUDA graph; replaying it
+    # on new inputs gives the same bits as a direct call on those inputs
+    w = mi.custom("graph", 1, 400, 3, 64, "uniform", seed_id=214)
+    d = to_dev(mi.make_inputs(w))
+    ws = mla.alloc_workspace(w.B, w.T, w.H, w.K)
+    out = torch.empty((w.B, w.T, w.H, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.B, w.T, w.H), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):   # first call outside the capture (per-device set-up)
+        mla.sparse_prefill(d["q"], d["c_kv"], d["k_pe"], d["gamma"], d["wkv_b"], d["topk_idx"], out=out, lse=lse,
+                           workspace=ws, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        mla.sparse_prefill(d["q"], d["c_kv"], d["k_pe"], d["gamma"], d["wkv_b"], d["topk_idx"], out=out, lse=lse,
+                           workspace=ws, stream=s)
+    d2 = to_dev(mi.make_inputs(mi.custom("graph2", 1, 400, 3, 64, "uniform", seed_id=215)))
+    for k in ("q", "c_kv", "k_pe", "gamma", "wkv_b", "topk_idx"):
+        d[k].copy_(d2[k])
+    g.replay()
+    torch.cuda.synchronize()
+    ref_out, ref_lse = mla.sparse_prefill(d2["q"], d2["c_kv"], d2["k_pe"], d2["gamma"], d2["wkv_b"], d2["topk_idx"])
+    torch.cuda.synchronize()
+    assert mla.get_status() == 0
+    assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
 
 
 @pytest.mark.parametrize("name", ["tiny", "headline", "long_context"])
