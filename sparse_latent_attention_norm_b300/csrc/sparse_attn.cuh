@@ -19,8 +19,9 @@
 //   softmax: four threads per query row (TMEM lane), 32 key columns each: apply the row's
 //           selection bits, block max of the raw scores (combined across the four threads with
 //           shared atomicMax), running max in the log2 domain with lazy rescaling (only when the
-//           max grows by more than 8 log2 units, with an exact power-of-two shift of the block's
-//           exponents in between), p = 2^(s * scale * log2 e - m) evaluated in fp16
+//           max grows by more than 8 log2 units; in between, a block above the running max is
+//           shifted so that its largest key's exponent is exactly 0), p = 2^(s * scale * log2 e
+//           - m) evaluated in fp16
 //           (ex2.approx.f16x2) and written to TMEM (64 cols of fp16 pairs).
 //   PV    : O[128 x 128] += P[128 x 128] . V[128 x 128], 8 UMMAs kind::f16 with P (fp16) read
 //           from TMEM and V (fp16) from shared memory (MN-major), O in TMEM (128 cols).
@@ -87,14 +88,15 @@ constexpr uint32_t TM_O = 256;          // O at cols 256..383
 constexpr uint32_t TM_QN = 384;         // q_nope as fp16 pairs, cols 384..447
 constexpr uint32_t TM_P = 448;          // P as fp16 pairs, cols 448..511
 // Online softmax in the log2 domain against a lagging reference max m. O and l are rescaled
-// (a TMEM round trip of O) only when a block's max exceeds m by more than RESCALE_THRESHOLD log2
-// units. Between rescales a block's exponents x = s * scale * log2 e - m can reach 8, where fp16
-// x carries an absolute error up to 2^-9 (1.4e-3 nats of lse on a row that one key carries). So
-// each row also takes an integer shift c >= 0 that brings x - c to at most X_MAX: p = 2^(x - c)
-// in fp16 (x - c with absolute error <= 2^-12, p with relative error <= 2^-11: lse within about
-// 7e-4 nats), then P = p * 2^c, exact in fp16 (an exponent shift), so P and l stay relative to m.
+// (a TMEM round trip of O) only when a block's max mb exceeds m by more than RESCALE_THRESHOLD
+// log2 units. In between, a block whose max lies above m is shifted: with c = mb - m, each row
+// exponentiates x - c = s * scale * log2 e - mb <= 0 in fp16, so the block's (and, once it is the
+// row's, the row's) largest key gets p = 2^0 = 1 exactly. ex2.approx.f16x2 is not correctly
+// rounded (up to one fp16 unit, ~1e-3 relative, measured over every fp16 input): a row that one
+// key carries would take that error into lse if the key's exponent were anywhere but 0. The row
+// sum adds the block's p in fp32 times 2^c in fp32 (lse keeps the exact weight of the largest
+// key); P for the PV UMMA is p * fp16(2^c) in fp16 (two roundings of 2^-11, seen only in out).
 constexpr float RESCALE_THRESHOLD = 8.0f;
-constexpr float X_MAX = 1.0f;
 constexpr float Q8_SCALE = 1.0f / 2048.0f; // 2^-11, undoes the 2^11 on k_lo
 
 struct Params {
@@ -658,29 +660,32 @@ __global__ void __launch_bounds__(THREADS, 1)
         const float alpha = need_o ? ex2(m_ref - mb) : 1.0f;
         if (need_o) l *= alpha;
         if (need) m_ref = mb;
-        // integer shift of this row's exponents (0 after a rescale and while no key is selected);
-        // mb <= m_ref + RESCALE_THRESHOLD here, so 0 <= c <= RESCALE_THRESHOLD - X_MAX = 7
-        const float c_shift = (mb == -INFINITY || m_ref == -INFINITY) ? 0.f : fmaxf(0.f, ceilf(mb - m_ref - X_MAX));
+        // shift of this row's exponents: 0 after a rescale, while no key is selected and when the
+        // block's max lies below m; mb <= m_ref + RESCALE_THRESHOLD here, so 0 <= c <= 8
+        const float c_shift = (mb == -INFINITY || m_ref == -INFINITY) ? 0.f : fmaxf(0.f, mb - m_ref);
         const float neg_m = (m_ref == -INFINITY) ? 0.f : -(m_ref + c_shift);   // no key yet: every p is 0
-        // p = 2^x with x = s * scale * log2 e - m - c <= 1 rounded to fp16 and exponentiated two at a
+        // p = 2^x with x = s * scale * log2 e - m - c rounded to fp16 and exponentiated two at a
         // time in fp16 (P is consumed as fp16 by the PV UMMA); l sums the same fp16 values in
-        // fp32, so out = O / l divides by exactly the weights O was built from.
+        // fp32 (times 2^c in fp32 when the block is shifted).
         uint32_t pk[PCOLS / 2];
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < PCOLS / 2; ++c)
           pk[c] = ex2_f16x2(pack_f16x2(fmaf(s[2 * c], sl2, neg_m), fmaf(s[2 * c + 1], sl2, neg_m)));
         if (__any_sync(0xffffffffu, c_shift > 0.f)) {
-          // P = p * 2^c: 2^c (c <= 7) is exact in fp16 and so is the product (an exponent shift;
-          // p <= 2, so P <= 256)
-          const uint32_t two_c = pack_f16x2(__int_as_float((127 + static_cast<int>(c_shift)) << 23),
-                                            __int_as_float((127 + static_cast<int>(c_shift)) << 23));
+          // l += 2^c * sum p (fp32); P = p * 2^c in fp16 (p <= 1, so P <= 256)
+          const float tc = ex2(c_shift);
+          const uint32_t two_c = pack_f16x2(tc, tc);
+#pragma unroll
+          for (int c = 0; c < PCOLS / 2; ++c) ls[c & 3] = add_f16x2_to_f32(pk[c], ls[c & 3]);
+          l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) * tc;
 #pragma unroll
           for (int c = 0; c < PCOLS / 2; ++c) pk[c] = hmul2_bits(pk[c], two_c);
-        }
+        } else {
 #pragma unroll
-        for (int c = 0; c < PCOLS / 2; ++c) ls[c & 3] = add_f16x2_to_f32(pk[c], ls[c & 3]);
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          for (int c = 0; c < PCOLS / 2; ++c) ls[c & 3] = add_f16x2_to_f32(pk[c], ls[c & 3]);
+          l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        }
         if (i > 0) {
           // P's TMEM columns and O are free once PV(g-1) has completed (for a tile's first block
           // the previous tile's epilogue waited for that). A failed wait here is carried into the

@@ -96,13 +96,14 @@ def test_full_size_every_element(mla, oracle_lib, name):
         del ref_out, ref_lse
 
 
-def lazy_rescale_inputs(T=256, H=128, K=16):
-    """Rows whose softmax sits on one key that scores well above the first key block's maximum,
-    with |lse| near or below 1: the score tail of q (feature 128) is b_h for head h and q's first
-    128 features are 0, so score_j = scale * b_h * a_j with a_j the first rotary feature of key j.
-    Keys 0..7 (first key block) have a_j = -1; key t >= 128 has a_t swept over [0, 1]; query t >= 128
-    selects {0..7, t}. Over the heads and rows, the gap between the dominant score and the first
-    block's maximum sweeps about 1 to 16 log2 units, crossing the online softmax's rescale point."""
+def lazy_rescale_inputs(n_early=8, a_lo=0.0, T=256, H=128, K=16):
+    """Rows whose softmax sits on one key that scores above the first key block's maximum, with
+    |lse| near or below 1: the score tail of q (feature 128) is b_h for head h and q's first 128
+    features are 0, so score_j = scale * b_h * a_j with a_j the first rotary feature of key j.
+    Keys 0..n_early-1 (first key block) have a_j = -1; key t >= 128 has a_t swept over
+    [a_lo, 1]; query t >= 128 selects {0..n_early-1, t}. Over the heads and rows, the gap between
+    the dominant score and the first block's maximum sweeps from under 1 to about 16 log2 units,
+    crossing any lag the online softmax lets its reference maximum have."""
     w = mi.custom("lazy_rescale", 1, T, H, K, "uniform", seed_id=210)
     inp = mi.make_inputs(w)
     q = torch.zeros((1, T, H, 192), dtype=torch.float32)
@@ -110,10 +111,10 @@ def lazy_rescale_inputs(T=256, H=128, K=16):
     q[0, :, :, 128] = b[None, :]
     k_pe = torch.zeros((1, T, 64), dtype=torch.float32)
     k_pe[0, :128, 0] = -1.0
-    k_pe[0, 128:, 0] = torch.linspace(0.0, 1.0, T - 128)
+    k_pe[0, 128:, 0] = torch.linspace(a_lo, 1.0, T - 128)
     topk = np.full((1, T, K), -1, dtype=np.int32)
     for t in range(T):
-        early = [j for j in range(8) if j <= t]
+        early = [j for j in range(n_early) if j <= t]
         row = early + ([t] if t >= 128 else [])
         topk[0, t, :len(row)] = row
     inp["q"] = q.to(torch.bfloat16)
@@ -122,13 +123,14 @@ def lazy_rescale_inputs(T=256, H=128, K=16):
     return inp
 
 
-def test_lse_rows_dominated_by_a_late_key(mla, oracle_lib):
-    # the online softmax keeps a reference maximum that lags the true one until a block's maximum
-    # exceeds it by the rescale threshold; a dominant late key then carries the whole row sum, so
-    # the precision of its weight is the precision of lse ("Keys" page, MHA prefill: softmax over
-    # the masked scores; lse is its log normaliser)
-    inp = lazy_rescale_inputs()
-    res = run_and_compare(mla, oracle_lib, inp, what="lazy rescale rows")
+@pytest.mark.parametrize("n_early,a_lo", [(8, 0.0), (1, -0.5)])
+def test_lse_rows_dominated_by_a_late_key(mla, oracle_lib, n_early, a_lo):
+    # an online softmax that lets its reference maximum lag the true one puts a dominant late key's
+    # exponent above 0, where fp16 spacing and the approximate exponential cost the most; that key
+    # carries the row sum, so the precision of its weight is the precision of lse ("Keys" page,
+    # MHA prefill: softmax over the masked scores; lse is its log normaliser)
+    inp = lazy_rescale_inputs(n_early, a_lo)
+    res = run_and_compare(mla, oracle_lib, inp, what=f"lazy rescale rows ({n_early} early keys)")
     assert res["rows"] == 256
 
 
