@@ -127,6 +127,17 @@ __device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
   return y;
 }
 
+// a * b + c on two fp32 lanes at once (each lane an IEEE fma, as fmaf).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t r;
+  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+      "mov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\tmov.b64 rc, {%5, %6};\n\t"
+      "fma.rn.f32x2 %0, ra, rb, rc;\n\t}"
+      : "=l"(r)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return make_float2(__uint_as_float(static_cast<uint32_t>(r)), __uint_as_float(static_cast<uint32_t>(r >> 32)));
+}
+
 // Elementwise product of two fp16 pairs, rounded to nearest.
 __device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
   uint32_t r;
@@ -670,8 +681,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t pk[PCOLS / 2];
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < PCOLS / 2; ++c)
-          pk[c] = ex2_f16x2(pack_f16x2(fmaf(s[2 * c], sl2, neg_m), fmaf(s[2 * c + 1], sl2, neg_m)));
+        for (int c = 0; c < PCOLS / 2; ++c) {
+          const float2 xx = fma2(make_float2(s[2 * c], s[2 * c + 1]), make_float2(sl2, sl2), make_float2(neg_m, neg_m));
+          pk[c] = ex2_f16x2(pack_f16x2(xx.x, xx.y));
+        }
         if (__any_sync(0xffffffffu, c_shift > 0.f)) {
           // l += 2^c * sum p (fp32); P = p * 2^c in fp16 (p <= 1, so P <= 256)
           const float tc = ex2(c_shift);
