@@ -75,13 +75,19 @@ def _code_only(text: str) -> str:
     return "".join(text.split())
 
 
-def kernel_sources_sha256() -> str:
-    """sha256 over the code of libmla's kernel sources and header (the inputs of every kernel
-    build), comments and whitespace excluded."""
+# the files the attention kernel's code comes from (its device code, the PTX helpers it calls and
+# the header whose constants it reads)
+ATTENTION_SOURCES = ("sparse_attn.cuh", "ptx.cuh")
+
+
+def kernel_sources_sha256(files=None) -> str:
+    """sha256 over the code of libmla's kernel sources (all of them, or the csrc files named in
+    `files`) and its header, comments and whitespace excluded."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_latent_attention_norm_b300", "csrc")
-    paths = [os.path.join(csrc, f) for f in sorted(os.listdir(csrc)) if f.endswith((".cu", ".cuh", ".h"))]
+    names = sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")) and (files is None or f in files))
+    paths = [os.path.join(csrc, f) for f in names]
     for path in paths + [os.path.join(ROOT, "include", "mla.h")]:
         h.update(os.path.basename(path).encode())
         with open(path, encoding="utf-8") as fh:
@@ -94,14 +100,15 @@ def profiled_traffic(workload: str):
     summary of the headline workload, or None when that capture predates the current sources."""
     if workload != "headline":
         return None
-    path = os.path.join(ROOT, "profiles", "kernels_headline_full.md")
+    path = os.path.join(ROOT, "profiles", "sparse_attn_headline.md")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         for line in f:
             if line.startswith("traffic: "):
                 kv = dict(x.split("=", 1) for x in line.split()[1:] if "=" in x)
-                if kv.get("kernel") == "sparse_attn_kernel" and kv.get("sources_sha256") == kernel_sources_sha256():
+                if kv.get("kernel") == "sparse_attn_kernel" and \
+                        kv.get("sources_sha256") == kernel_sources_sha256(ATTENTION_SOURCES):
                     return int(kv["dram_bytes_per_launch"])
     return None
 
@@ -147,10 +154,14 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
+    _count = 0
+
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join("/tmp", f"mla_clocks_{os.getpid()}.csv")
+        ClockSampler._count += 1   # one file per sampler: a later sampler must not overwrite it
+        self.path = os.path.join("/tmp", f"mla_clocks_{os.getpid()}_{ClockSampler._count}.csv")
+        self._summary = None
 
     def __enter__(self):
         try:
@@ -197,10 +208,13 @@ class ClockSampler:
                 "reasons": sorted(seen), "samples": len(rows)}
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        with open(self.path) as f:
-            return self.parse(f)
+        if self._summary is None:
+            if self.proc is None or not os.path.exists(self.path):
+                self._summary = {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+            else:
+                with open(self.path) as f:
+                    self._summary = self.parse(f)
+        return self._summary
 
 
 def cpu_baseline(inp, w, seconds_hint: float = 15.0, threads: int = 0):
@@ -439,9 +453,27 @@ def run_ours(args, rank, world, dist):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    # --options: the step with the model's own steps around the MHA excerpt (for profilers)
+    opt_kw, wkv = {}, d["wkv_b"]
+    if args.options:
+        names = set(args.options.split(","))
+        if "fp8_wkv_b" in names:
+            w8, scale = fp8_weight_of(d["wkv_b"])
+            opt_kw["wkv_b_scale"] = scale
+            wkv = w8
+        if "fp8_latent" in names:
+            opt_kw["fp8_latent"] = True
+            opt_kw["kv_cache"] = torch.empty((B, T, 512), dtype=torch.bfloat16, device=dev)
+            opt_kw["pe_cache"] = torch.empty((B, T, 64), dtype=torch.bfloat16, device=dev)
+        if "rope" in names:
+            opt_kw["rope"] = True
+        ws = mla.alloc_workspace(B, T, H, K, device=dev,
+                                 opt=mla.options(flags=mla.FLAG_ROPE if opt_kw.get("rope") else 0,
+                                                 wkv_b_scale=opt_kw.get("wkv_b_scale")))
+
     def step():
-        mla.sparse_prefill(d["q"], d["c_kv"], d["k_pe"], d["gamma"], d["wkv_b"], d["topk_idx"], out=out, lse=lse,
-                           workspace=ws, stream=stream)
+        mla.sparse_prefill(d["q"], d["c_kv"], d["k_pe"], d["gamma"], wkv, d["topk_idx"], out=out, lse=lse,
+                           workspace=ws, stream=stream, **opt_kw)
 
     # selected-key count for the formula (outside any timed region)
     _, _, nk = mla.sparse_prefill(d["q"], d["c_kv"], d["k_pe"], d["gamma"], d["wkv_b"], d["topk_idx"],
@@ -468,6 +500,7 @@ def run_ours(args, rank, world, dist):
             step()
             ends[i].record(stream)
         torch.cuda.synchronize()
+    main_clocks = clocks.summary()
     barrier(dist)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = max_over_ranks(sum(step_ms) / len(step_ms), dist)
@@ -589,7 +622,7 @@ def run_ours(args, rank, world, dist):
         "variants": variants,
         "per_config": per_config,
         "gpu_launches": 3 * args.steps,
-        "clocks": clocks.summary(),
+        "clocks": main_clocks,
     }
     print(json.dumps(line), flush=True)
 
@@ -609,6 +642,8 @@ def main():
                     help="seconds of back-to-back steps for the sustained figure (0: skip)")
     ap.add_argument("--config-steps", type=int, default=10, help="timed steps per other workload")
     ap.add_argument("--no-per-config", action="store_true", help="time the chosen workload only")
+    ap.add_argument("--options", default="",
+                    help="with --kernels-only: comma list of fp8_wkv_b, fp8_latent, rope to switch on (profilers)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, dist = dist_setup()

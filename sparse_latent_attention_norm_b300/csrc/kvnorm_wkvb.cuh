@@ -161,6 +161,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_w);
+    // the c_kv rows of this CTA's row tiles go to L2 now, so the RMSNorm's loads hit L2
+    const int m0 = u_begin / (2 * p.H), m1 = (u_end - 1) / (2 * p.H);
+    for (int m = m0; m <= m1 && m < p.n_mtiles; ++m) {
+      const int b = m / p.mt_per_b, t0 = (m % p.mt_per_b) * BM;
+      const int rows = min(BM, p.T - t0);
+      const uint16_t* src = p.c_kv + (static_cast<int64_t>(b) * p.T + t0) * KDIM;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(static_cast<uint32_t>(rows * KDIM * 2))
+                   : "memory");
+    }
   }
   tc_fence_before();
   __syncthreads();

@@ -65,12 +65,13 @@ def test_profiled_traffic_tracks_kernel_sources(tmp_path, monkeypatch):
     assert bench.profiled_traffic("tiny") is None
     prof = tmp_path / "profiles"
     prof.mkdir()
-    (prof / "kernels_headline_full.md").write_text(
-        "x\ntraffic: kernel=sparse_attn_kernel dram_bytes_per_launch=123 sources_sha256=%s\n" % bench.kernel_sources_sha256())
+    (prof / "sparse_attn_headline.md").write_text(
+        "x\ntraffic: kernel=sparse_attn_kernel dram_bytes_per_launch=123 sources_sha256=%s\n"
+        % bench.kernel_sources_sha256(bench.ATTENTION_SOURCES))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setattr(bench, "kernel_sources_sha256", lambda: "0" * 64)
+    monkeypatch.setattr(bench, "kernel_sources_sha256", lambda files=None: "0" * 64)
     assert bench.profiled_traffic("headline") is None
-    (prof / "kernels_headline_full.md").write_text(
+    (prof / "sparse_attn_headline.md").write_text(
         "traffic: kernel=sparse_attn_kernel dram_bytes_per_launch=123 sources_sha256=%s\n" % ("0" * 64))
     assert bench.profiled_traffic("headline") == 123
 
