@@ -596,6 +596,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     bool ok = true;
     int g = 0;        // global block counter of this CTA
+    int slot3 = 0;    // g % 3: the max_key slot of block g
     int it = 0;
     int item = -1;
     {
@@ -624,21 +625,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (i + 1 < tl.nblk)
           mask_next = (row_valid && in_bounds((i + 1) * 4 + part < p.W && tl.b < p.B)) ? __ldg(bits_row + (i + 1) * 4) : 0u;
         const int sb = g & 1;
-        const int slot = g % 3;
+        const int slot = slot3;
         bool got = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (g >> 1) & 1, abort_p));
         float s[PCOLS];
         if (got) {
           tc_fence_after();
           if (__any_sync(0xffffffffu, mask != 0u)) {
-            uint32_t v[PCOLS];
-            tmem_ld_32x32b_x32(tmem + lane_off + TM_S + static_cast<uint32_t>(sb * BK + part * PCOLS), v);
+            tmem_ld_32x32b_x32(tmem + lane_off + TM_S + static_cast<uint32_t>(sb * BK + part * PCOLS),
+                               *reinterpret_cast<uint32_t(*)[PCOLS]>(s));
             tmem_ld_wait();
-            if (__all_sync(0xffffffffu, mask == 0xFFFFFFFFu)) {   // every key of the part selected
+            if (!__all_sync(0xffffffffu, mask == 0xFFFFFFFFu)) {   // some key of the part unselected
 #pragma unroll
-              for (int e = 0; e < PCOLS; ++e) s[e] = __uint_as_float(v[e]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < PCOLS; ++e) s[e] = ((mask >> e) & 1u) ? __uint_as_float(v[e]) : -INFINITY;
+              for (int e = 0; e < PCOLS; ++e) s[e] = ((mask >> e) & 1u) ? s[e] : -INFINITY;
             }
           } else {
 #pragma unroll
@@ -665,7 +663,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const float mb = float_from_order_key(max_key[slot][r]) * sl2;
         // the slot of block g-1 has been read by every warp of the quadrant (each read it before
         // arriving at this block's barrier); it is next written at block g+2, after the next barrier
-        if (part == 0 && g > 0) max_key[(g + 2) % 3][r] = INT_MIN;
+        if (part == 0 && g > 0) max_key[slot3 == 0 ? 2 : slot3 - 1][r] = INT_MIN;
+        slot3 = (slot3 == 2) ? 0 : slot3 + 1;
         const bool need = mb > m_ref + RESCALE_THRESHOLD;   // true on the first selected key
         const bool need_o = need && (m_ref != -INFINITY);   // O and l hold earlier blocks' mass
         const float alpha = need_o ? ex2(m_ref - mb) : 1.0f;
