@@ -140,7 +140,8 @@ def canon_row(idx: np.ndarray, t: int) -> np.ndarray:
     return sel[:n].copy()
 
 
-def prefill(inputs: dict, rows=None, heads=None, threads: int = 0, rope: bool = False, fp8_latent: bool = False):
+def prefill(inputs: dict, rows=None, heads=None, threads: int = 0, rope: bool = False, fp8_latent: bool = False,
+            emulate_bf16: bool = False):
     """Run the oracle prefill.
 
     ``inputs`` holds q [B,T,H,192], c_kv [B,T,512], k_pe [B,T,64] (bf16), gamma [512] fp32,
@@ -149,6 +150,9 @@ def prefill(inputs: dict, rows=None, heads=None, threads: int = 0, rope: bool = 
     numpy arrays). ``rows``: flat row ids b*T+t (default: all). ``heads``: (h_begin, h_end)
     (default: all). ``rope``: q[..., 128:] and k_pe are unrotated and get YaRN RoPE at their
     positions. ``fp8_latent``: the normalised latent goes through the KV cache's FP8 round trip.
+    ``emulate_bf16``: the diagnostic rounding-emulation mode (the pages' bf16 tensors rounded where
+    the MHA prefill excerpt would hold them: wkv_b's output, the scores before and after the scale,
+    the softmax weights, out); not a parity reference.
     Returns (out [R,Hs,128] fp64, lse [R,Hs] fp64, n_keys [R] int32).
     """
     q = _bits(inputs["q"])
@@ -177,7 +181,7 @@ def prefill(inputs: dict, rows=None, heads=None, threads: int = 0, rope: bool = 
     out = np.empty((nr, h1 - h0, V), dtype=np.float64)
     lse = np.empty((nr, h1 - h0), dtype=np.float64)
     nk = np.empty(nr, dtype=np.int32)
-    opts = (1 if rope else 0) | (2 if fp8_latent else 0)
+    opts = (1 if rope else 0) | (2 if fp8_latent else 0) | (4 if emulate_bf16 else 0)
     rc = _load().oracle_prefill_opt(B, T, H, K, _ptr(q), _ptr(c_kv), _ptr(k_pe), _ptr(g),
                                     None if W is None else _ptr(W), None if W8 is None else _ptr(W8),
                                     None if Ws is None else _ptr(Ws), _ptr(topk), nr,

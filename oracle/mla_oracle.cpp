@@ -351,7 +351,11 @@ int oracle_canon_row(const int32_t* idx, int K, int t, int32_t* sel) {
 //   rows   flat row ids b*T + t, n_rows of them; NULL means all B*T rows in order
 //   heads  [h_begin, h_end)
 //   opts   bit 0: rotate q[..., 128:192] at position t and k_pe at position j (YaRN RoPE, the
-//          inputs then being unrotated); bit 1: FP8 round trip of the normalised latent
+//          inputs then being unrotated); bit 1: FP8 round trip of the normalised latent;
+//          bit 2: rounding emulation, a diagnostic of the pages' own bf16 arithmetic: wkv_b's
+//          output, the scores before and after the scale, the softmax weights and out are
+//          rounded to bf16 where the MHA prefill excerpt's bf16 tensors would hold them (lse is
+//          taken from the rounded scores)
 //   out    fp64 [n_rows, h_end - h_begin, 128];  lse fp64 [n_rows, h_end - h_begin];
 //   n_keys int32 [n_rows] (may be NULL)
 // Returns 0, or -1 on a bad argument.
@@ -362,7 +366,7 @@ int oracle_prefill_opt(int B, int T, int H, int K, const uint16_t* q, const uint
                        int threads) {
   if (B < 1 || T < 1 || H < 1 || K < 1 || h_begin < 0 || h_end > H || h_begin >= h_end) return -1;
   if (W8 != nullptr && W_scale == nullptr) return -1;
-  const bool rope = (opts & 1) != 0, fp8_latent = (opts & 2) != 0;
+  const bool rope = (opts & 1) != 0, fp8_latent = (opts & 2) != 0, emulate = (opts & 4) != 0;
   const int64_t BT = static_cast<int64_t>(B) * T;
   std::vector<int64_t> row_ids;
   if (rows == nullptr) {
@@ -420,9 +424,12 @@ int oracle_prefill_opt(int B, int T, int H, int K, const uint16_t* q, const uint
     head_weight_t(W, W8, W_scale, h, wt);
     const int npos = tmax[b] + 1;
     std::vector<double> kv(static_cast<size_t>(npos) * kKV);  // [j][k_nope 128 | v 128]
-    for (int j = 0; j < npos; ++j)
-      up_proj_row(y.data() + (static_cast<int64_t>(b) * T + j) * kLatent, wt.data(),
-                  kv.data() + static_cast<size_t>(j) * kKV);
+    for (int j = 0; j < npos; ++j) {
+      double* kvj = kv.data() + static_cast<size_t>(j) * kKV;
+      up_proj_row(y.data() + (static_cast<int64_t>(b) * T + j) * kLatent, wt.data(), kvj);
+      if (emulate)   // kv = self.wkv_b(kv): a bf16 Linear's output
+        for (int f = 0; f < kKV; ++f) kvj[f] = round_to_bf16(kvj[f]);
+    }
     std::vector<double> s;
     for (int64_t i : rows_of_batch[b]) {
       const int64_t r = row_ids[i];
@@ -454,7 +461,8 @@ int oracle_prefill_opt(int B, int T, int H, int K, const uint16_t* q, const uint
         double dot = 0.0;
         for (int d = 0; d < kNope; ++d) dot += qh[d] * kn[d];
         for (int d = 0; d < kRope; ++d) dot += qh[kNope + d] * kp[d];
-        s[a] = dot * scale;
+        // einsum(q, k) into a bf16 tensor, then .mul_(softmax_scale) in bf16 (emulation)
+        s[a] = emulate ? round_to_bf16(round_to_bf16(dot) * scale) : dot * scale;
       }
       // softmax over the selected keys, then the value mix.
       double M = s[0];
@@ -465,12 +473,22 @@ int oracle_prefill_opt(int B, int T, int H, int K, const uint16_t* q, const uint
         Z += x;
       }
       for (int d = 0; d < kV; ++d) o[d] = 0.0;
-      for (size_t a = 0; a < S.size(); ++a) {
-        const double* vj = kv.data() + static_cast<size_t>(S[a]) * kKV + kNope;
-        const double p = s[a];
-        for (int d = 0; d < kV; ++d) o[d] += p * vj[d];
+      if (emulate) {
+        // scores.softmax(-1) into bf16 weights, einsum with v into a bf16 out
+        for (size_t a = 0; a < S.size(); ++a) {
+          const double* vj = kv.data() + static_cast<size_t>(S[a]) * kKV + kNope;
+          const double p = round_to_bf16(s[a] / Z);
+          for (int d = 0; d < kV; ++d) o[d] += p * vj[d];
+        }
+        for (int d = 0; d < kV; ++d) o[d] = round_to_bf16(o[d]);
+      } else {
+        for (size_t a = 0; a < S.size(); ++a) {
+          const double* vj = kv.data() + static_cast<size_t>(S[a]) * kKV + kNope;
+          const double p = s[a];
+          for (int d = 0; d < kV; ++d) o[d] += p * vj[d];
+        }
+        for (int d = 0; d < kV; ++d) o[d] /= Z;
       }
-      for (int d = 0; d < kV; ++d) o[d] /= Z;
       *l = M + std::log(Z);
     }
   });

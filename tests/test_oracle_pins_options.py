@@ -245,3 +245,34 @@ def test_prefill_fp8_latent_attends_over_the_round_tripped_latent(oracle_lib):
         assert np.allclose(lse[:, h], m[:, 0] + np.log(p.sum(axis=1)), rtol=1e-12, atol=1e-12)
     out0, _, _ = oracle_lib.prefill(inp)
     assert not np.array_equal(out, out0)
+
+
+# ------------------------------------------------------- rounding emulation (diagnostic mode)
+def test_emulation_with_zero_queries_is_the_rounded_mean(oracle_lib):
+    # q = 0 makes every score 0 exactly: the pages' bf16 softmax gives every selected key the bf16
+    # value of 1/n, out is bf16(bf16(1/n) * sum of the bf16-rounded v), lse = ln n
+    w = mi.custom("pin_emul", 1, 40, 2, 40, "dense", seed_id=35)
+    inp = mi.make_inputs(w)
+    inp["q"] = torch.zeros_like(inp["q"])
+    out, lse, nk = oracle_lib.prefill(inp, emulate_bf16=True)
+    y = oracle_lib.kv_norm(inp["c_kv"].reshape(-1, 512), inp["gamma"].numpy())
+    _, v = oracle_lib.up_proj(y, inp["wkv_b"])                      # [T, H, 128], exact
+    vb = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    for t in range(w.T):
+        n = t + 1
+        p = float(torch.tensor(1.0 / n, dtype=torch.float64).to(torch.bfloat16).to(torch.float64))
+        want = torch.from_numpy(p * vb[:n].sum(axis=0)).to(torch.bfloat16).to(torch.float64).numpy()
+        assert np.array_equal(out[t], want)
+        assert np.allclose(lse[t], math.log(n), rtol=0, atol=1e-12)
+
+
+def test_emulation_outputs_are_bf16_and_near_the_exact_result(oracle_lib):
+    w = mi.custom("pin_emul2", 1, 200, 3, 48, "uniform", seed_id=36)
+    inp = mi.make_inputs(w)
+    out, lse, _ = oracle_lib.prefill(inp)
+    oe, le, _ = oracle_lib.prefill(inp, emulate_bf16=True)
+    assert np.array_equal(oracle_lib.round_to_bf16(oe), oe)
+    assert not np.array_equal(oe, out)
+    # bf16 keeps 8 significant bits: each rounding moves a value by at most 2^-9 of itself
+    assert np.abs(oe - out).max() <= 0.1 * max(1.0, np.abs(out).max())
+    assert np.abs(le - lse).max() <= 2.0 ** -6 * max(1.0, np.abs(lse).max())
