@@ -373,3 +373,23 @@ def test_threads_do_not_change_bits(oracle_lib):
     b = oracle_lib.prefill(inp, threads=5)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+def test_kv_norm_agrees_with_torch_running_the_excerpt(oracle_lib):
+    # torch's own fp32 execution of the RMSNorm excerpt ("Key-value RMSNorm" page, model.py
+    # 281-293: x.float(), x.pow(2).mean(-1, keepdim=True), x * torch.rsqrt(var + eps), weight * x,
+    # .to(dtype)) sums the squares in its own order and uses its own rsqrt: the oracle's fixed
+    # order (ascending features, 1 / sqrt) is one fp32 reading of the same step. The bf16 outputs
+    # may differ only where an fp32 result lies next to a bf16 rounding boundary: by one bf16 unit,
+    # on a small fraction of the elements.
+    inp = small_inputs(B=1, T=2048, H=1, K=4, stress=True, seed=41)
+    x = inp["c_kv"].reshape(-1, 512)
+    gamma = inp["gamma"]
+    ref = oracle_lib.kv_norm(x, gamma.numpy())
+    xf = x.float()
+    var = xf.pow(2).mean(-1, keepdim=True)
+    yt = (gamma * (xf * torch.rsqrt(var + 1e-6))).to(torch.bfloat16).to(torch.float64).numpy()
+    diff = np.abs(yt - ref)
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
+    assert (diff <= ulp * 1.0001).all()
+    assert (diff > 0).mean() < 0.01
