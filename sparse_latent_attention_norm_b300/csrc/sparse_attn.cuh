@@ -357,6 +357,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             const Tile nt = tile_of(next, p);
             tma_prefetch_l2_4d(&tm_q, 0, nt.h, nt.t0, nt.b);
             tma_prefetch_l2_4d(&tm_q, 64, nt.h, nt.t0, nt.b);
+            if (p.rope_cs != nullptr) {
+              // RoPE mode: the query warps also read the unrotated q_pe and the (cos, sin) rows
+              tma_prefetch_l2_4d(&tm_q, 128, nt.h, nt.t0, nt.b);
+              const int rows = min(BQ, p.T - nt.t0);
+              asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.rope_cs + static_cast<int64_t>(nt.t0) * 32),
+                           "r"(static_cast<uint32_t>(rows * 32 * 8))
+                           : "memory");
+            }
           }
         }
       }
