@@ -89,28 +89,49 @@ __device__ __forceinline__ float max_nan(float a, float b) {
   return r;
 }
 
+// Up to n tries of mbarrier.try_wait on phase `parity` in one PTX loop (two instructions per
+// failed try besides the count); true as soon as one succeeds.
+__device__ __forceinline__ bool mbar_try_wait_n(uint64_t* bar, uint32_t parity, uint32_t n) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b32 k;\n\t"
+      "mov.b32 k, %3;\n"
+      "WAIT_AGAIN:\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "@p bra WAIT_DONE;\n\t"
+      "sub.u32 k, k, 1;\n\t"
+      "setp.ne.u32 q, k, 0;\n\t"
+      "@q bra WAIT_AGAIN;\n"
+      "WAIT_DONE:\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(n)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait on phase `parity`. Returns false (after recording a timeout) when the limit
-// passes, or at once when `abort_flag` (shared, may be null) is already set by another thread.
+// passes, or when `abort_flag` (shared, may be null) has been set by another thread or another
+// CTA has recorded a timeout. These are checked, with the clock, between runs of 256 tries,
+// which keeps the spinning thread's loop short: the waiting warps share their SM sub-partition's
+// issue slots with the softmax warps.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  uint32_t spins = 0;
-  while (!mbar_try_wait(bar, parity)) {
+  for (;;) {
+    if (mbar_try_wait_n(bar, parity, 256u)) return true;
     if (abort_flag && *abort_flag) return false;
-    if ((++spins & 255u) == 0u) {
-      // another CTA already timed out: unwind now instead of waiting out this CTA's own limit
-      if (*(volatile unsigned int*)&g_status & (1u << kErrTimeout)) {
-        if (abort_flag) *abort_flag = 1;
-        return false;
-      }
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        set_error(kErrTimeout);
-        if (abort_flag) *abort_flag = 1;
-        return false;
-      }
+    // another CTA already timed out: unwind now instead of waiting out this CTA's own limit
+    if (*(volatile unsigned int*)&g_status & (1u << kErrTimeout)) {
+      if (abort_flag) *abort_flag = 1;
+      return false;
+    }
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      set_error(kErrTimeout);
+      if (abort_flag) *abort_flag = 1;
+      return false;
     }
   }
-  return true;
 }
 
 // ------------------------------------------ TMA ----------------------------------------------

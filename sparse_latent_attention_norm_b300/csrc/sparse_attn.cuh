@@ -128,14 +128,15 @@ __device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
 }
 
 // a * b + c on two fp32 lanes at once (each lane an IEEE fma, as fmaf).
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  uint64_t r;
-  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
-      "mov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\tmov.b64 rc, {%5, %6};\n\t"
-      "fma.rn.f32x2 %0, ra, rb, rc;\n\t}"
-      : "=l"(r)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return make_float2(__uint_as_float(static_cast<uint32_t>(r)), __uint_as_float(static_cast<uint32_t>(r >> 32)));
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+// x if bit `bit` (a one-bit constant) of `mask` is set, else -inf.
+__device__ __forceinline__ float keep_if_bit(float x, uint32_t mask, uint32_t bit) {
+  asm("{\n\t.reg .pred p;\n\t.reg .b32 t;\n\tand.b32 t, %1, %2;\n\tsetp.ne.u32 p, t, 0;\n\t"
+      "selp.f32 %0, %0, 0fFF800000, p;\n\t}"
+      : "+f"(x)
+      : "r"(mask), "r"(bit));
+  return x;
 }
 
 // Elementwise product of two fp16 pairs, rounded to nearest.
@@ -644,7 +645,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_ld_wait();
             if (!__all_sync(0xffffffffu, mask == 0xFFFFFFFFu)) {   // some key of the part unselected
 #pragma unroll
-              for (int e = 0; e < PCOLS; ++e) s[e] = ((mask >> e) & 1u) ? s[e] : -INFINITY;
+              for (int e = 0; e < PCOLS; ++e) s[e] = keep_if_bit(s[e], mask, 1u << e);
             }
           } else {
 #pragma unroll
