@@ -109,10 +109,12 @@ cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 mla_status launch_canon(const int32_t* topk_idx, mla_dims d, uint32_t* sel_bits, int32_t* n_keys, unsigned flags,
                         uint32_t* sched, cudaStream_t st) {
   const int W = bits_words(d.T);
-  const size_t smem = static_cast<size_t>(W) * 4;
-  const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(d.B) * d.T);
-  mla::canon_select_kernel<<<grid, mla::kCanonThreads, smem, st>>>(topk_idx, d.T, d.K, W, sel_bits, n_keys,
-                                                                   (flags & MLA_FLAG_VALIDATE_INDICES) ? 1 : 0, sched);
+  const int rows_per_cta = mla::canon_rows_per_cta(W);
+  const size_t smem = static_cast<size_t>(rows_per_cta) * W * 4;
+  const int64_t rows = static_cast<int64_t>(d.B) * d.T;
+  const unsigned grid = static_cast<unsigned>((rows + rows_per_cta - 1) / rows_per_cta);
+  mla::canon_select_kernel<<<grid, 32 * rows_per_cta, smem, st>>>(topk_idx, rows, d.T, d.K, W, sel_bits, n_keys,
+                                                                  (flags & MLA_FLAG_VALIDATE_INDICES) ? 1 : 0, sched);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -58,6 +58,7 @@ SMALL = [
     ("dense_small", mi.custom("dense_small", 1, 200, 2, 256, "dense", seed_id=204)),
     ("single_query", mi.custom("single_query", 1, 1, 3, 4, "tiny", seed_id=205)),
     ("one_tile_edge", mi.custom("one_tile_edge", 1, 129, 1, 16, "uniform", seed_id=206)),
+    ("odd_topk_width", mi.custom("odd_topk_width", 1, 300, 3, 37, "uniform", stress=True, seed_id=207)),
 ]
 
 
@@ -208,9 +209,19 @@ def test_prefill_captured_in_a_cuda_graph(mla):
     assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
 
 
-@pytest.mark.parametrize("name", ["tiny", "headline", "long_context"])
+# top-k widths that are not a multiple of 4 take the selection stage's scalar index loads; widths
+# above 1,024 (vector loads) or 256 (scalar) take more than one batch of loads per lane
+SELECTION_CASES = {
+    "tiny": mi.custom("sel", 2, 300, 1, 80, "uniform", stress=True, seed_id=7),
+    "odd_k": mi.custom("sel_odd", 1, 300, 1, 37, "uniform", stress=True, seed_id=8),
+    "odd_k_wide": mi.custom("sel_odd_wide", 2, 700, 1, 301, "uniform", stress=True, seed_id=9),
+    "wide_k": mi.custom("sel_wide", 1, 1500, 1, 1100, "uniform", stress=True, seed_id=10),
+}
+
+
+@pytest.mark.parametrize("name", ["tiny", "odd_k", "odd_k_wide", "wide_k", "headline", "long_context"])
 def test_selection_bitsets_bit_exact(mla, oracle_lib, name):
-    w = mi.WORKLOADS[name] if name != "tiny" else mi.custom("sel", 2, 300, 1, 80, "uniform", stress=True, seed_id=7)
+    w = SELECTION_CASES[name] if name in SELECTION_CASES else mi.WORKLOADS[name]
     topk = mi.make_topk(w)
     if name == "tiny":
         topk[0, 5, :10] = [-3, 299, 300, 10_000, 5, 5, 4, -1, 6, 7]   # out of range, non-causal, dups
