@@ -348,10 +348,17 @@ def sparse_attention(q, k_pe, kv, klo, sel_bits, *, rope_cs=None, stream=None):
     return out, lse
 
 
+# The model's weights (kv_norm's gain and wkv_b) and the per-step activations of the prefill.
+WEIGHTS = ("gamma", "wkv_b")
+ACTIVATIONS = ("q", "c_kv", "k_pe", "topk_idx")
+
+
 class HostPrefill:
     """End-to-end use from host memory: per call, copy the inputs from (pinned) host tensors to the
     device, run mla_sparse_prefill and copy out / lse back to pinned host tensors. Device buffers
-    and the workspace are allocated once for the shapes given at construction."""
+    and the workspace are allocated once for the shapes given at construction. After
+    set_weights(gamma, wkv_b) the weights stay on the device and a call copies the activations
+    (q, c_kv, k_pe, topk_idx) only."""
 
     def __init__(self, B: int, T: int, H: int, K: int, device="cuda"):
         import torch
@@ -370,9 +377,20 @@ class HostPrefill:
         self.ws = alloc_workspace(B, T, H, K, device=dev)
         self.out_h = torch.empty(self.out.shape, dtype=torch.bfloat16, pin_memory=True)
         self.lse_h = torch.empty(self.lse.shape, dtype=torch.float32, pin_memory=True)
+        self.resident = False
+
+    def set_weights(self, gamma, wkv_b) -> None:
+        """Copy the weights to the device once; later calls copy the activations only."""
+        self.d["gamma"].copy_(gamma)
+        self.d["wkv_b"].copy_(wkv_b)
+        self.resident = True
+
+    def _copied(self):
+        return ACTIVATIONS if self.resident else ACTIVATIONS + WEIGHTS
 
     def h2d_bytes(self, inputs) -> int:
-        return sum(inputs[k].numel() * inputs[k].element_size() for k in self.d)
+        """Bytes a call copies host -> device."""
+        return sum(inputs[k].numel() * inputs[k].element_size() for k in self._copied())
 
     def d2h_bytes(self) -> int:
         return self.out.numel() * 2 + self.lse.numel() * 4
@@ -383,8 +401,8 @@ class HostPrefill:
         import torch
         s = torch.cuda.current_stream() if stream is None else stream
         with torch.cuda.stream(s):
-            for k, dst in self.d.items():
-                dst.copy_(inputs[k], non_blocking=True)
+            for k in self._copied():
+                self.d[k].copy_(inputs[k], non_blocking=True)
             sparse_prefill(self.d["q"], self.d["c_kv"], self.d["k_pe"], self.d["gamma"], self.d["wkv_b"],
                            self.d["topk_idx"], out=self.out, lse=self.lse, workspace=self.ws, stream=s)
             self.out_h.copy_(self.out, non_blocking=True)
@@ -405,7 +423,9 @@ class HostPrefillPipeline:
         h = pipe.submit(inputs)          # returns at once
         out, lse = pipe.result(h)        # waits for that step's results on the host
 
-    The host tensors a step returns are reused `depth` submissions later."""
+    The host tensors a step returns are reused `depth` submissions later. After
+    set_weights(gamma, wkv_b) the weights stay on the device (one copy shared by the buffer sets)
+    and a step copies the activations (q, c_kv, k_pe, topk_idx) only."""
 
     def __init__(self, B: int, T: int, H: int, K: int, device="cuda", depth: int = 2):
         import torch
@@ -433,13 +453,30 @@ class HostPrefillPipeline:
                 "out_free": None,   # event: that step's results have reached the host
             })
         self.ws = alloc_workspace(B, T, H, K, device=self.dev)
+        self.weights = None   # device (gamma, wkv_b) once set_weights has run
         self.s_h2d = torch.cuda.Stream(device=self.dev)
         self.s_comp = torch.cuda.Stream(device=self.dev)
         self.s_d2h = torch.cuda.Stream(device=self.dev)
         self.n = 0
 
+    def set_weights(self, gamma, wkv_b) -> None:
+        """Copy the weights to the device once (ordered before every later step); later steps
+        copy the activations only."""
+        import torch
+        w = {"gamma": torch.empty_like(self.slots[0]["in"]["gamma"]),
+             "wkv_b": torch.empty_like(self.slots[0]["in"]["wkv_b"])}
+        with torch.cuda.stream(self.s_h2d):
+            w["gamma"].copy_(gamma, non_blocking=True)
+            w["wkv_b"].copy_(wkv_b, non_blocking=True)
+        self.s_h2d.synchronize()
+        self.weights = w
+
+    def _copied(self):
+        return ACTIVATIONS if self.weights is not None else ACTIVATIONS + WEIGHTS
+
     def h2d_bytes(self, inputs) -> int:
-        return sum(inputs[k].numel() * inputs[k].element_size() for k in self.slots[0]["in"])
+        """Bytes a step copies host -> device."""
+        return sum(inputs[k].numel() * inputs[k].element_size() for k in self._copied())
 
     def d2h_bytes(self) -> int:
         o = self.slots[0]
@@ -454,14 +491,14 @@ class HostPrefillPipeline:
         if slot["in_free"] is not None:
             self.s_h2d.wait_event(slot["in_free"])
         with torch.cuda.stream(self.s_h2d):
-            for k, dst in slot["in"].items():
-                dst.copy_(inputs[k], non_blocking=True)
+            for k in self._copied():
+                slot["in"][k].copy_(inputs[k], non_blocking=True)
         copied = torch.cuda.Event()
         copied.record(self.s_h2d)
         self.s_comp.wait_event(copied)
         if slot["out_free"] is not None:
             self.s_comp.wait_event(slot["out_free"])
-        d = slot["in"]
+        d = dict(slot["in"], **self.weights) if self.weights is not None else slot["in"]
         sparse_prefill(d["q"], d["c_kv"], d["k_pe"], d["gamma"], d["wkv_b"], d["topk_idx"], out=slot["out"],
                        lse=slot["lse"], workspace=self.ws, stream=self.s_comp)
         computed = torch.cuda.Event()

@@ -338,6 +338,39 @@ def test_pipelined_host_path_matches_direct_calls(mla):
     assert mla.get_status() == 0
 
 
+def test_host_paths_with_resident_weights(mla):
+    # the weights go to the device once; the steps copy their activations only and give the same
+    # results as direct device calls with those weights
+    ws = [mi.custom("resident", 1, 300, 2, 48, "uniform", seed_id=50 + i) for i in range(4)]
+    inps = [mi.make_inputs(w) for w in ws]
+    for inp in inps[1:]:
+        inp["gamma"], inp["wkv_b"] = inps[0]["gamma"], inps[0]["wkv_b"]
+    refs = []
+    for inp in inps:
+        d = to_dev(inp)
+        o, l = mla.sparse_prefill(d["q"], d["c_kv"], d["k_pe"], d["gamma"], d["wkv_b"], d["topk_idx"])
+        refs.append((o.cpu(), l.cpu()))
+    hosts = [{k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()} for inp in inps]
+    pipe = mla.HostPrefillPipeline(1, 300, 2, 48)
+    full = pipe.h2d_bytes(hosts[0])
+    pipe.set_weights(hosts[0]["gamma"], hosts[0]["wkv_b"])
+    assert pipe.h2d_bytes(hosts[0]) == full - hosts[0]["gamma"].numel() * 4 - hosts[0]["wkv_b"].numel() * 2
+    handles = [pipe.submit(hosts[0]), pipe.submit(hosts[1])]
+    for i in range(2, 4):
+        out, lse = pipe.result(handles[i - 2])
+        assert torch.equal(out, refs[i - 2][0]) and torch.equal(lse, refs[i - 2][1])
+        handles.append(pipe.submit(hosts[i]))
+    for i in (2, 3):
+        out, lse = pipe.result(handles[i])
+        assert torch.equal(out, refs[i][0]) and torch.equal(lse, refs[i][1])
+    hp = mla.HostPrefill(1, 300, 2, 48)
+    hp.set_weights(hosts[0]["gamma"], hosts[0]["wkv_b"])
+    for i in (1, 3):
+        out, lse = hp(hosts[i])
+        assert torch.equal(out, refs[i][0]) and torch.equal(lse, refs[i][1])
+    assert mla.get_status() == 0
+
+
 def test_run_on_side_stream(mla):
     w = mi.custom("stream", 1, 384, 2, 64, "uniform", seed_id=17)
     d = to_dev(mi.make_inputs(w))
