@@ -59,6 +59,7 @@ SMALL = [
     ("single_query", mi.custom("single_query", 1, 1, 3, 4, "tiny", seed_id=205)),
     ("one_tile_edge", mi.custom("one_tile_edge", 1, 129, 1, 16, "uniform", seed_id=206)),
     ("odd_topk_width", mi.custom("odd_topk_width", 1, 300, 3, 37, "uniform", stress=True, seed_id=207)),
+    ("batch8", mi.custom("batch8", 8, 200, 3, 32, "uniform", seed_id=208)),
 ]
 
 
@@ -122,6 +123,16 @@ def lazy_rescale_inputs(n_early=8, a_lo=0.0, T=256, H=128, K=16):
     inp["k_pe"] = k_pe.to(torch.bfloat16)
     inp["topk_idx"] = torch.from_numpy(topk)
     return inp
+
+
+def test_maximum_sequence_length(mla, oracle_lib):
+    # the longest sequence the library takes, T = 65,536: 512 query tiles per head with up to 512
+    # key blocks each, 2,048-word bitsets (six rows per selection CTA); tile edges, the last rows
+    # and seeded random rows against the oracle, their n_keys bit-exact
+    w = mi.custom("max_t", 1, 65536, 2, 256, "uniform", stress=True, seed_id=220)
+    inp = mi.make_inputs(w)
+    rows = parity.sample_rows(w.B, w.T, w.K, n_random=40, seed=3)
+    run_and_compare(mla, oracle_lib, inp, rows=rows, what="max_t")
 
 
 @pytest.mark.parametrize("n_early,a_lo", [(8, 0.0), (1, -0.5)])
