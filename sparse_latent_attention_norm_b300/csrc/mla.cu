@@ -65,15 +65,18 @@ mla_status device_setup(int* num_sms, int* k1_ctas) {
                              mla::k2::SMEM_BYTES) != cudaSuccess)
       return MLA_ERR_CUDA;
     {
-      // the GEMM stage's grid is a fixed set of CTAs with fixed unit ranges: launch no more CTAs
-      // than can be resident together
-      int per_sm = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mla::k1::kvnorm_wkvb_kernel, mla::k1::THREADS,
-                                                        mla::k1::SMEM_BYTES) != cudaSuccess) {
-        per_sm = 0;
+      // the GEMM stage's grid is a fixed set of CTA pairs with fixed unit ranges: launch no more
+      // pairs than can be resident together
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2, 1, 1);
+      cfg.blockDim = dim3(mla::k1::THREADS, 1, 1);
+      cfg.dynamicSmemBytes = mla::k1::SMEM_BYTES;
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, mla::k1::kvnorm_wkvb_kernel, &cfg) != cudaSuccess) {
+        clusters = 0;
         (void)cudaGetLastError();   // the query's error is not the caller's
       }
-      d.k1_ctas = per_sm * d.num_sms;
+      d.k1_ctas = 2 * clusters;
     }
     d.ready = true;
   }
@@ -125,7 +128,7 @@ mla_status launch_kvnorm_wkvb(const mla_bf16* c_kv, const float* gamma, const ml
   {
     const uint64_t dims[2] = {kLatent, static_cast<uint64_t>(d.H) * kKV};
     const uint64_t strides[1] = {kLatent * 2};
-    const uint32_t box[2] = {64, mla::k1::BN};
+    const uint32_t box[2] = {64, mla::k1::BNH};
     if (!mla::make_tmap_bf16(&tm_w, wkv_b, 2, dims, strides, box)) return MLA_ERR_CUDA;
   }
   mla::k1::Params p;
@@ -134,9 +137,11 @@ mla_status launch_kvnorm_wkvb(const mla_bf16* c_kv, const float* gamma, const ml
   p.H = d.H;
   p.mt_per_b = (d.T + mla::k1::BM - 1) / mla::k1::BM;
   const int64_t n_mtiles = static_cast<int64_t>(d.B) * p.mt_per_b;
-  const int64_t units = n_mtiles * d.H * 2;
+  const int64_t n_tpairs = (n_mtiles + 1) / 2;
+  const int64_t units = n_tpairs * d.H;
   if (units > INT32_MAX / 2) return MLA_ERR_UNSUPPORTED;
   p.n_mtiles = static_cast<int>(n_mtiles);
+  p.n_tpairs = static_cast<int>(n_tpairs);
   p.units = static_cast<int>(units);
   p.c_kv = c_kv;
   p.gamma = gamma;
@@ -145,9 +150,12 @@ mla_status launch_kvnorm_wkvb(const mla_bf16* c_kv, const float* gamma, const ml
   p.fp8_latent = fp8_latent ? 1 : 0;
   p.kv_cache = kv_cache;
   p.cache_len = cache_len;
-  // no more CTAs than can be resident at once (each CTA's range of units is fixed)
-  int grid = k1_max_ctas > 0 ? k1_max_ctas : num_sms;
-  if (grid > p.units) grid = p.units;
+  // CTA pairs (clusters of two), no more than can be resident at once (each pair's range of
+  // units is fixed)
+  int pairs = k1_max_ctas > 0 ? k1_max_ctas / 2 : num_sms / 2;
+  if (pairs > p.units) pairs = p.units;
+  if (pairs < 1) pairs = 1;
+  const int grid = 2 * pairs;
   mla::k1::kvnorm_wkvb_kernel<<<grid, mla::k1::THREADS, mla::k1::SMEM_BYTES, st>>>(tm_w, p);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
