@@ -394,6 +394,31 @@ def test_run_on_side_stream(mla):
     assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
 
 
+def test_concurrent_calls_on_four_streams(mla):
+    # four prefills with their own inputs and workspaces enqueued on four streams at once (the
+    # GEMM stage's CTA pairs and the persistent attention CTAs of different calls interleave on
+    # the SMs): each result equals the same call made alone
+    shapes = [(1, 700, 3, 64), (2, 333, 5, 48), (1, 1100, 2, 128), (1, 129, 4, 16)]
+    inps = [to_dev(mi.make_inputs(mi.custom(f"conc{i}", *sh, "uniform", seed_id=60 + i))) for i, sh in enumerate(shapes)]
+    refs = []
+    for d in inps:
+        o, l = mla.sparse_prefill(d["q"], d["c_kv"], d["k_pe"], d["gamma"], d["wkv_b"], d["topk_idx"])
+        refs.append((o, l))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in inps]
+    wss = [mla.alloc_workspace(*sh) for sh in shapes]
+    outs = []
+    for d, s, ws in zip(inps, streams, wss):
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            outs.append(mla.sparse_prefill(d["q"], d["c_kv"], d["k_pe"], d["gamma"], d["wkv_b"], d["topk_idx"],
+                                           workspace=ws, stream=s))
+    torch.cuda.synchronize()
+    assert mla.get_status() == 0
+    for (o, l), (ro, rl) in zip(outs, refs):
+        assert torch.equal(o, ro) and torch.equal(l, rl)
+
+
 def test_gpu_error_is_below_the_pages_own_bf16_rounding(mla, oracle_lib):
     # diagnostic: the oracle's rounding-emulation mode reproduces the pages' bf16 tensors; the
     # library, measured against the exact oracle, stays closer than that emulation on lse and on
