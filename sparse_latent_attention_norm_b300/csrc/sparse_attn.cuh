@@ -71,7 +71,7 @@ constexpr int TILE_BYTES = QPE_BYTES + Q8_BYTES + NK_STAGE * K_BYTES + NV_STAGE 
 struct Ctrl {
   int max_key[3][BQ];        // [block % 3][row]: block max of the row's selected raw scores, as an
                              // order-preserving integer key, reduced with shared atomicMax
-  int item_idx[2];           // tile indices published by the K producer (-1: no more tiles)
+  int4 item_pub[2];          // tiles published by the K producer: {index (-1: no more tiles), b, h, qt}
   uint64_t item_full[2], item_empty[2];
   uint64_t q_full, q_ready, q_free, o_free, drain, drain_pv;
   uint64_t k_full[NK_STAGE], k_empty[NK_STAGE];
@@ -287,13 +287,20 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = tmem_base;
 
   // Every role walks the same tile sequence: tile number `it` of this CTA is published in slot
-  // it & 1 of item_idx by the K producer. take_item returns the tile index (or -1 past the end)
-  // and releases the slot; false if the wait gave up.
-  auto take_item = [&](int it, int& item) -> bool {
+  // it & 1 of item_pub by the K producer, with its (batch, head, query tile) worked out once.
+  // take_item returns the tile index (or -1 past the end) and the tile, and releases the slot;
+  // false if the wait gave up.
+  auto take_item = [&](int it, int& item, Tile& tl) -> bool {
     const int slot = it & 1;
     if (!mbar_wait(&item_full[slot], (it >> 1) & 1, abort_p)) return false;
-    item = ctl.item_idx[slot];
+    const int4 v = ctl.item_pub[slot];
     mbar_arrive(&item_empty[slot]);
+    item = v.x;
+    tl.b = v.y;
+    tl.h = v.z;
+    tl.qt = v.w;
+    tl.t0 = v.w * BQ;
+    tl.nblk = v.w + 1;
     return true;
   };
 
@@ -314,11 +321,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int item = next < p.n_items ? next : -1;
         const int slot = it & 1;
         if (it >= 2 && !mbar_wait(&item_empty[slot], ((it - 2) >> 1) & 1, abort_p)) { ok = false; break; }
-        ctl.item_idx[slot] = item;
+        Tile tl{};
+        if (item >= 0) tl = tile_of(item, p);
+        ctl.item_pub[slot] = make_int4(item, tl.b, tl.h, tl.qt);
         mbar_arrive(&item_full[slot]);
         if (item < 0) break;
         next = static_cast<int>(atomicAdd(p.sched, 1u));
-        const Tile tl = tile_of(item, p);
         const int kv_plane = tl.b * p.H + tl.h;
         // q_pe of this tile replaces the previous tile's once its last QK^T has completed
         if (it >= 1 && !mbar_wait(&q_free, (it - 1) & 1, abort_p)) { ok = false; break; }
@@ -387,9 +395,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t vph = 0;
       for (int it = 0; ok; ++it) {
         int item;
-        if (!take_item(it, item)) { ok = false; break; }
+        Tile tl;
+        if (!take_item(it, item, tl)) { ok = false; break; }
         if (item < 0) break;
-        const Tile tl = tile_of(item, p);
         const int kv_plane = tl.b * p.H + tl.h;
         for (int i = 0; i < tl.nblk; ++i) {
           if (!mbar_wait(&v_empty[vs], vph ^ 1, abort_p)) { ok = false; break; }
@@ -434,9 +442,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       int g = 0;   // global block counter of this CTA
       for (int it = 0; ok; ++it) {
         int item;
-        if (!take_item(it, item)) break;
+        Tile tl;
+        if (!take_item(it, item, tl)) break;
         if (item < 0) break;
-        const Tile tl = tile_of(item, p);
         if (!mbar_wait(&q_full, it & 1, abort_p) || !mbar_wait(&q_ready, it & 1, abort_p)) break;
         for (int i = 0; i < tl.nblk; ++i, ++g) {
           const int sb = g & 1;
@@ -485,9 +493,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       int g = 0;
       for (int it = 0; ok; ++it) {
         int item;
-        if (!take_item(it, item)) break;
+        Tile tl;
+        if (!take_item(it, item, tl)) break;
         if (item < 0) break;
-        const Tile tl = tile_of(item, p);
         // O is rewritten from the tile's first block on: the previous tile's epilogue must have read it
         if (it >= 1 && !mbar_wait(&o_free, (it - 1) & 1, abort_p)) break;
         for (int i = 0; i < tl.nblk; ++i, ++g) {
@@ -608,19 +616,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     int slot3 = 0;    // g % 3: the max_key slot of block g
     int it = 0;
     int item = -1;
+    Tile cur{};
     {
-      const bool got = take_item(0, item);
+      const bool got = take_item(0, item, cur);
       ok = quad_sync_and(quad_bar, got);
     }
     uint32_t first_mask = 0u;   // selection word of the first block of the tile about to start
     if (ok && item >= 0) {
-      const Tile t0l = tile_of(item, p);
+      const Tile& t0l = cur;
       const int tt = t0l.t0 + r;
       first_mask = (tt < p.T && in_bounds(t0l.b < p.B)) ? __ldg(p.sel_bits + (static_cast<int64_t>(t0l.b) * p.T + tt) * p.W + part) : 0u;
       prepare_queries(t0l);
     }
     while (ok && item >= 0) {
-      const Tile tl = tile_of(item, p);
+      const Tile tl = cur;
       const int t = tl.t0 + r;
       const bool row_valid = t < p.T;
       // this thread's selection word of block i: keys PCOLS*part .. +31 of the block
@@ -735,12 +744,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       // The next tile's queries go in now, so its first QK^T blocks overlap this tile's epilogue:
       // every QK^T of this tile has completed (its last scores were read above).
       int next_item = -1;
+      Tile nt{};
       {
-        const bool got = take_item(it + 1, next_item);
+        const bool got = take_item(it + 1, next_item, nt);
         ok = quad_sync_and(quad_bar, got);
       }
       if (ok && next_item >= 0) {
-        const Tile nt = tile_of(next_item, p);
         const int nt_t = nt.t0 + r;
         // the next tile's first selection word, loaded now so its latency passes during the
         // query preparation and this tile's epilogue
@@ -789,6 +798,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       item = next_item;
+      cur = nt;
       ++it;
     }
   }
